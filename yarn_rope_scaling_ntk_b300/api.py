@@ -1,0 +1,237 @@
+"""Python binding of ``libyarn_attn.so`` (ctypes).
+
+Argument marshalling only: tensors become raw pointers and strides, the
+caller's current CUDA stream is passed through, and every step of the path
+runs in the library's kernels.  PyTorch provides device memory (outputs and
+workspaces) and streams.  There is no CPU fallback: if the library is missing
+or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libyarn_attn.so"
+
+KIND = {"none": 0, "plain": 1, "pi": 2, "ntk": 3, "yarn": 4}
+MASK = {"causal": 0, "sink_window": 1, "none": 2}
+F32, BF16 = 0, 1
+STATUS = {0: "YR_OK", 1: "YR_ERR_INVALID_ARG", 2: "YR_ERR_UNSUPPORTED", 3: "YR_ERR_CUDA",
+          4: "YR_ERR_TIMEOUT"}
+
+
+class YarnAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("theta_base", ctypes.c_double), ("L_train", ctypes.c_int32),
+                ("L_target", ctypes.c_int32), ("s", ctypes.c_double),
+                ("ramp_alpha", ctypes.c_double), ("ramp_beta", ctypes.c_double),
+                ("mscale_override", ctypes.c_double)]
+
+
+@dataclass(frozen=True)
+class RopeConfig:
+    """The pages' problem statement: rescaling kind, head dim d, base b,
+    L_train, L_target, scale s (<= 0: L_target / L_train), YaRN ramp bounds
+    and an optional temperature override."""
+    kind: str = "yarn"
+    head_dim: int = 128
+    theta_base: float = 10000.0
+    L_train: int = 0
+    L_target: int = 0
+    s: float = 0.0
+    ramp_alpha: float = 1.0
+    ramp_beta: float = 32.0
+    mscale_override: float = 0.0
+
+    def c(self) -> _Cfg:
+        if self.kind not in KIND:
+            raise ValueError(f"unknown rope kind {self.kind!r}")
+        return _Cfg(KIND[self.kind], int(self.head_dim), float(self.theta_base), int(self.L_train),
+                    int(self.L_target), float(self.s), float(self.ramp_alpha),
+                    float(self.ramp_beta), float(self.mscale_override))
+
+
+_lib = None
+_i64x3 = ctypes.c_int64 * 3
+_P = ctypes.c_void_p
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing; build it with `python -m yarn_rope_scaling_ntk_b300.build`")
+    lib = ctypes.CDLL(path)
+    I32, SZ, D = ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
+    cfgp = ctypes.POINTER(_Cfg)
+    sig = {
+        "yarn_inv_freq": (I32, [cfgp, ctypes.POINTER(D), ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(D)]),
+        "rope_apply": (I32, [cfgp, _P, _P, I32, I32, I32, I32, I32, _i64x3, _i64x3, I32, _P, I32, _P]),
+        "yr_prefill_workspace_bytes": (SZ, [cfgp, I32, I32, I32, I32, I32, I32]),
+        "attn_fwd_prefill": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32, I32,
+                                   _i64x3, _i64x3, _i64x3, _i64x3, I32, I32, I32, I32,
+                                   ctypes.c_float, _P, SZ, _P]),
+        "yr_decode_auto_splits": (I32, [I32, I32, I32, I32]),
+        "yr_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
+        "attn_fwd_decode_sinkwindow": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
+                                             I32, _P, _P, I32, _P, SZ, _P]),
+        "yr_sync_status": (I32, [_P]),
+        "yr_last_error_message": (ctypes.c_char_p, []),
+        "yr_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _check(st: int):
+    if st != 0:
+        raise YarnAttnError(st, load_library().yr_last_error_message().decode())
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _strides(t: torch.Tensor):
+    if t.stride(-1) != 1:
+        raise ValueError("the last (head-dim) axis must be contiguous")
+    return _i64x3(*t.stride()[:3])
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def yarn_inv_freq(cfg: RopeConfig):
+    """Host-only: (theta'[d/2] float64, classes[d/2] int8, mscale)."""
+    lib = load_library()
+    h = cfg.head_dim // 2
+    th = (ctypes.c_double * h)()
+    cl = (ctypes.c_int8 * h)()
+    ms = ctypes.c_double()
+    c = cfg.c()
+    _check(lib.yarn_inv_freq(ctypes.byref(c), th, cl, ctypes.byref(ms)))
+    return np.array(th[:], dtype=np.float64), np.array(cl[:], dtype=np.int8), ms.value
+
+
+def rope_apply(cfg: RopeConfig, x: torch.Tensor, out: torch.Tensor | None = None,
+               positions: torch.Tensor | None = None, pos0: int = 0, apply_mscale: bool = False,
+               stream=None) -> torch.Tensor:
+    """Rotate x [B, H, S, d] (float32 or bfloat16); ``out`` may be ``x``."""
+    lib = load_library()
+    if x.dim() != 4:
+        raise ValueError("x must be [B, H, S, d]")
+    y = torch.empty_like(x) if out is None else out
+    if positions is not None and (positions.dtype != torch.int32 or positions.device != x.device):
+        raise ValueError("positions must be an int32 tensor on x's device")
+    B, H, S, d = x.shape
+    c = cfg.c()
+    _check(lib.rope_apply(ctypes.byref(c), _ptr(x), _ptr(y), _dtype_code(x), B, H, S, d,
+                          _strides(x), _strides(y), int(pos0), _ptr(positions),
+                          int(bool(apply_mscale)), _stream(stream)))
+    return y
+
+
+def prefill_workspace_bytes(cfg: RopeConfig, dtype: torch.dtype, B, Hq, Hkv, S, d) -> int:
+    c = cfg.c()
+    code = F32 if dtype == torch.float32 else BF16
+    return int(load_library().yr_prefill_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, S, d))
+
+
+def attn_fwd_prefill(cfg: RopeConfig, q, k, v, mask: str = "causal", sink: int = 0,
+                     window: int = 0, ring_blocks: int = 1, softmax_scale: float = 0.0,
+                     out=None, lse=None, return_lse: bool = False, workspace=None, stream=None):
+    """Exact attention with RoPE rescaling fused: q [B, Hq, S, d], k/v
+    [B, Hkv, S, d] (float32 or bfloat16).  Returns o (and lse [B, Hq, S])."""
+    lib = load_library()
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, S, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, S, d] matching q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k and v must share a dtype")
+    o = torch.empty_like(q) if out is None else out
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)
+    need = prefill_workspace_bytes(cfg, q.dtype, B, Hq, Hkv, S, d)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    c = cfg.c()
+    _check(lib.attn_fwd_prefill(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                _dtype_code(q), B, Hq, Hkv, S, d, _strides(q), _strides(k),
+                                _strides(v), _strides(o), MASK[mask], int(sink), int(window),
+                                int(ring_blocks), float(softmax_scale), _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
+    return (o, lse) if return_lse else o
+
+
+def decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits=0) -> int:
+    return int(load_library().yr_decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits))
+
+
+def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ring_start,
+                               sink: int, window: int, num_splits: int = 0, out=None, lse=None,
+                               return_lse: bool = False, workspace=None, stream=None):
+    """q [B, Hq, d] bf16; caches [B, Hkv, sink + window, d] bf16 (contiguous);
+    n_valid / ring_start int32 [B].  Returns o [B, Hq, d] (and lse [B, Hq])."""
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    for t in (q, k_cache, v_cache):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q and the caches must be contiguous bfloat16")
+    if k_cache.shape != (B, Hkv, sink + window, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [B, Hkv, sink + window, d]")
+    for t in (n_valid, ring_start):
+        if t.dtype != torch.int32 or t.shape != (B,):
+            raise ValueError("n_valid and ring_start must be int32 [B]")
+    o = torch.empty_like(q) if out is None else out
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    c = cfg.c()
+    _check(lib.attn_fwd_decode_sinkwindow(
+        ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(n_valid), _ptr(ring_start),
+        B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return (o, lse) if return_lse else o
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise if a device-side bounded wait gave up."""
+    _check(load_library().yr_sync_status(_stream(stream)))

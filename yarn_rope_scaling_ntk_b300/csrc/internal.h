@@ -1,0 +1,80 @@
+// Private declarations shared by the host entry points and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "yarn_attn.h"
+
+namespace yr {
+
+constexpr int kMaxHalf = 128;  // d/2 upper bound for rope_apply (d <= 256)
+
+// Per-dimension rotation rate in turns per position, theta'_i / (2 pi), split
+// into a float hi part and a float lo remainder so that the device can form
+// the fractional turn m * f exactly enough for float32 outputs (positions are
+// exact integers below 2^24).
+struct RopeFreqs {
+  float2 f[kMaxHalf];  // x = hi, y = lo
+  float mscale;        // temperature factor (1 when not YaRN)
+  int32_t half;        // d / 2
+  int32_t identity;    // 1 when every frequency is zero (kind NONE)
+};
+
+// Host: validate cfg for head dimension d and fill the float64 frequencies.
+yr_status compute_inv_freq(const yr_rope_cfg* cfg, int d, double* theta, int8_t* cls,
+                           double* mscale);
+// Host: the device table built from compute_inv_freq.
+yr_status build_rope_freqs(const yr_rope_cfg* cfg, int d, RopeFreqs* out);
+
+// Error text helpers (thread-local message).
+yr_status fail(yr_status st, const char* fmt, ...);
+void clear_error();
+yr_status cuda_fail(cudaError_t e, const char* what);
+
+// Address of the device status word (per device), set by bounded waits.
+int* device_status_word();
+
+// ---- launches (kernel files) ----------------------------------------------
+struct RopeLaunch {
+  const void* x;
+  void* y;
+  int in_bf16, out_bf16;
+  int B, H, S, d;
+  int64_t xs[3], ys[3];
+  int pos0;
+  const int32_t* positions;
+  int apply_mscale;
+  int precise;  // 1: sincospif-based angles (float32 outputs)
+};
+cudaError_t launch_rope(const RopeLaunch& a, const RopeFreqs& f, cudaStream_t st);
+
+struct DecodeLaunch {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const int32_t* n_valid;
+  const int32_t* ring_start;
+  void* o;
+  float* lse;
+  float* ws;  // split partials (NULL when splits == 1)
+  int B, Hq, Hkv, d, sink, window, splits;
+  float scale_log2;
+};
+cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
+
+struct PrefillLaunch {
+  const void* q;  // bf16 rotated (or raw when rotate_q_in_kernel)
+  const void* k;  // bf16 rotated
+  const void* v;  // bf16
+  void* o;
+  float* lse;
+  int out_bf16;
+  int B, Hq, Hkv, S, d;
+  int64_t qs[3], ks[3], vs[3], os[3];
+  int mask, sink, window, ring_blocks;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t st);
+
+}  // namespace yr
