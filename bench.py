@@ -22,7 +22,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -70,53 +69,59 @@ def cfg_of(w):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event reasons sampled through NVML every 5 ms on a
+    background thread (read-only queries) while the timed region runs."""
+
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4}
 
     def __init__(self, index: int):
         self.index = index
         self.rows = []
-        self.proc = None
+        self.stop = threading.Event()
         self.thread = None
+        self.h = None
 
     def __enter__(self):
-        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            # the CUDA device's own NVML handle (CUDA_VISIBLE_DEVICES may remap indices)
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
         except Exception:
-            self.proc = None
+            self.h = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 7:
-                self.rows.append(parts)
+    def _run(self):
+        nv = self.nv
+        while not self.stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                try:
+                    rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                except Exception:
+                    rs = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+                self.rows.append((sm, rs))
+            except Exception:
+                pass
+            time.sleep(0.005)
 
     def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self.stop.set()
         if self.thread:
             self.thread.join(timeout=2)
 
     def summary(self):
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].strip() == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+        reasons = sorted({n for _, r in self.rows for n, bit in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(sm for sm, _ in self.rows), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.rows), "source": "NVML, 5 ms"}
 
 
 def timed(fn, steps: int, stream) -> list:
@@ -335,6 +340,36 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_part(args):
+    """One kernel family alone, for profiling: ``--part prefill|decode|rope``
+    runs W + K calls of that entry point; ``--small`` shrinks the workload
+    (prefill S=4096, decode B=8) while keeping inputs larger than L2."""
+    from dataclasses import replace
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = max(1, args.warmup) + max(1, args.steps)
+    if args.part in ("prefill", "rope"):
+        w = W.LLAMA2_7B if not args.small else replace(W.LLAMA2_7B, S=4096, name="llama2_7b_shape_S4096")
+        cfg = cfg_of(w)
+        q, k, v = W.prefill_inputs(w, dev)
+        o = torch.empty_like(q)
+        ws = torch.empty(api.prefill_workspace_bytes(cfg, q.dtype, w.B, w.Hq, w.Hkv, w.S, w.d),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(n):
+            if args.part == "prefill":
+                api.attn_fwd_prefill(cfg, q, k, v, mask=w.mask, out=o, workspace=ws)
+            else:
+                api.rope_apply(cfg, q, out=o)
+    else:
+        wd = W.DECODE if not args.small else replace(W.DECODE, B=8, name="decode_B8")
+        dq, kc, vc, nv, rs = W.decode_inputs(wd, dev)
+        dcfg = api.RopeConfig(kind="plain", head_dim=wd.d, theta_base=wd.rope.theta_base)
+        for _ in range(n):
+            api.attn_fwd_decode_sinkwindow(dcfg, dq, kc, vc, nv, rs, wd.sink, wd.window)
+    api.sync_status()
+    print(json.dumps({"part": args.part, "small": args.small, "calls": n}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,8 +377,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=["prefill", "decode", "rope"], default=None,
+                    help="profile one kernel family alone (prints no bench line)")
+    ap.add_argument("--small", action="store_true", help="with --part: smaller workload")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.part:
+        run_part(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
