@@ -204,6 +204,29 @@ yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, cons
                                      void* o, float* lse, int32_t num_splits, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* attn_fwd_decode_sinkwindow without a workspace argument, for callers that
+ * cannot allocate device memory when they call (for example an engine's
+ * per-step hook that must not allocate, or a process whose device memory is
+ * all reserved by another allocator) or have no scratch buffer to pass.  The
+ * pages have no counterpart: this is an interface convenience only.
+ * Arguments, layouts and results are those of attn_fwd_decode_sinkwindow.
+ * The split partial states go to one fixed 4 MiB array of device memory that
+ * the library holds on every GPU that loads it, until the process exits; the
+ * call itself allocates nothing.  Its first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress, with the device current), so
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array and it keeps the last call's contents (each call writes
+ * every partial state before reading it); calls that overlap on the GPU
+ * race.  A split count whose scratch would exceed 4 MiB
+ * (num_splits * B * Hq * (d + 2) * 4 bytes) returns YR_ERR_INVALID_ARG with
+ * a message; a split count of 1 needs no scratch. */
+yr_status attn_fwd_decode_sinkwindow_noalloc(const yr_rope_cfg* cfg, const void* q,
+                                             const void* k_cache, const void* v_cache,
+                                             const int32_t* n_valid, const int32_t* ring_start,
+                                             int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                                             int32_t sink, int32_t window, void* o, float* lse,
+                                             int32_t num_splits, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set; returns YR_ERR_TIMEOUT if one gave up, YR_ERR_CUDA on a
  * CUDA error, YR_OK otherwise. */

@@ -94,6 +94,8 @@ def load_library():
         "yr_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
         "attn_fwd_decode_sinkwindow": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
                                              I32, _P, _P, I32, _P, SZ, _P]),
+        "attn_fwd_decode_sinkwindow_noalloc": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32,
+                                                     I32, I32, _P, _P, I32, _P]),
         "yr_sync_status": (I32, [_P]),
         "yr_last_error_message": (ctypes.c_char_p, []),
         "yr_version": (ctypes.c_char_p, []),
@@ -230,6 +232,24 @@ def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ri
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return (o, lse) if return_lse else o
+
+
+def attn_fwd_decode_sinkwindow_noalloc(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ring_start,
+                                       sink: int, window: int, num_splits: int = 0, out=None,
+                                       lse=None, stream=None):
+    """Decode without a workspace: the split scratch is the library's own
+    fixed 4 MiB device array (for callers that cannot allocate when they
+    call).  ``out`` and ``lse`` are the caller's; nothing is allocated when
+    both are given."""
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    o = torch.empty_like(q) if out is None else out
+    c = cfg.c()
+    _check(lib.attn_fwd_decode_sinkwindow_noalloc(
+        ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(n_valid), _ptr(ring_start),
+        B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits), _stream(stream)))
+    return o
 
 
 def sync_status(stream=None):

@@ -13,6 +13,8 @@
 // memory, and across slices by a second kernel.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -274,3 +276,69 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
 }
 
 }  // namespace yr
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode entry point.
+//
+// Some callers cannot hand the library a workspace: code that runs where
+// device allocation is not allowed at call time (for example an engine's
+// per-step enqueue hook that must not allocate, or a process whose memory is
+// entirely reserved by another allocator) and callers that have no scratch
+// buffer to spare.  For them the split-slice partial states live in one
+// fixed array of device memory that belongs to the library: every GPU that
+// loads the library holds it until the process exits.
+//
+// The array is shared by every call on a device and keeps the previous
+// call's contents; the decode kernel writes every partial state it later
+// merges, so nothing needs clearing between calls.  Calls whose work overlaps
+// on the GPU (other streams, or launches not ordered on one stream) race on
+// the array.
+namespace yr {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Device address of g_decode_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+float* decode_scratch_address() {
+  static std::mutex mu;
+  static float* cached[128] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<float*>(p);
+  }
+  return cached[dev];
+}
+
+}  // namespace
+}  // namespace yr
+
+extern "C" yr_status attn_fwd_decode_sinkwindow_noalloc(
+    const yr_rope_cfg* cfg, const void* q, const void* k_cache, const void* v_cache, const int32_t* n_valid,
+    const int32_t* ring_start, int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t sink, int32_t window,
+    void* o, float* lse, int32_t num_splits, void* stream) {
+  const size_t need = yr_decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits);
+  if (need > yr::kNoAllocScratchBytes) {
+    yr::clear_error();
+    return yr::fail(YR_ERR_INVALID_ARG,
+                    "attn_fwd_decode_sinkwindow_noalloc: %zu bytes of split scratch needed, above its fixed "
+                    "%zu-byte array; use fewer splits or attn_fwd_decode_sinkwindow with a workspace",
+                    need, yr::kNoAllocScratchBytes);
+  }
+  void* scratch = nullptr;
+  if (need > 0) {
+    scratch = yr::decode_scratch_address();
+    if (!scratch) {
+      yr::clear_error();
+      return yr::fail(YR_ERR_CUDA, "attn_fwd_decode_sinkwindow_noalloc: device scratch address unavailable");
+    }
+  }
+  return attn_fwd_decode_sinkwindow(cfg, q, k_cache, v_cache, n_valid, ring_start, B, Hq, Hkv, d, sink, window,
+                                    o, lse, num_splits, scratch, need, stream);
+}
