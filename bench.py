@@ -68,6 +68,43 @@ def cfg_of(w):
                           L_target=r.L_target, s=r.s)
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes on the driver's libnvidia-ml."""
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                self.lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            raise RuntimeError("libnvidia-ml not found")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        p = torch.cuda.get_device_properties(cuda_index)
+        bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+            raise RuntimeError(f"no NVML handle for {bus!r}")
+
+    def sm_clock(self, fn="nvmlDeviceGetClockInfo") -> int:
+        v = self.c.c_uint()
+        if getattr(self.lib, fn)(self.h, 1, self.c.byref(v)) != 0:  # 1 = NVML_CLOCK_SM
+            raise RuntimeError(fn)
+        return v.value
+
+    def reasons(self) -> int:
+        v = self.c.c_ulonglong()
+        for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            if hasattr(self.lib, fn) and getattr(self.lib, fn)(self.h, self.c.byref(v)) == 0:
+                return v.value
+        raise RuntimeError("clock event reasons unavailable")
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled through NVML every 5 ms on a
     background thread (read-only queries) while the timed region runs."""
@@ -80,35 +117,25 @@ class ClockSampler:
         self.rows = []
         self.stop = threading.Event()
         self.thread = None
-        self.h = None
+        self.error = None
+        self.max_mhz = None
 
     def __enter__(self):
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            # the CUDA device's own NVML handle (CUDA_VISIBLE_DEVICES may remap indices)
-            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(self.index)
+            self.max_mhz = self.nv.sm_clock("nvmlDeviceGetMaxClockInfo")
             self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
-        except Exception:
-            self.h = None
+        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.error = str(e)
         return self
 
     def _run(self):
-        nv = self.nv
         while not self.stop.is_set():
             try:
-                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                try:
-                    rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                except Exception:
-                    rs = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
-                self.rows.append((sm, rs))
-            except Exception:
-                pass
+                self.rows.append((self.nv.sm_clock(), self.nv.reasons()))
+            except Exception as e:  # noqa: BLE001
+                self.error = str(e)
             time.sleep(0.005)
 
     def __exit__(self, *exc):
@@ -118,7 +145,8 @@ class ClockSampler:
 
     def summary(self):
         if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "error": self.error}
         reasons = sorted({n for _, r in self.rows for n, bit in self.REASONS.items() if r & bit})
         return {"sm_mhz": statistics.median(sm for sm, _ in self.rows), "sm_max_mhz": self.max_mhz,
                 "reasons": reasons, "samples": len(self.rows), "source": "NVML, 5 ms"}

@@ -4,28 +4,53 @@
 // Scaling", Production defaults).  Keys are stored unrotated and rotated on
 // read at their logical cache index; the query sits at n_valid - 1.
 //
-// HBM-bound: every valid cache entry is read once with 16-byte loads.  A CTA
-// owns one (sequence, kv head) and one slice of the logical entries; TPK
-// threads share a key (each holds 8 rotation pairs: one 16-byte vector from
-// each half of the head dimension), and every key group keeps its own
-// online-softmax state (running max, sum, unnormalised output) in registers.
-// States are merged across the warp by shuffles, across warps in shared
-// memory, and across slices by a second kernel.
+// HBM-bound: every valid cache entry is read once.  A CTA owns one
+// (sequence, kv head) and one slice of the logical entries.  A producer warp
+// streams the slice in chunks of CK logical entries into a three-stage
+// shared-memory ring with bulk asynchronous copies (a chunk maps to at most
+// three physically contiguous runs: sinks, ring up to its wrap, ring after
+// the wrap), so the bytes in flight do not depend on registers.  Eight
+// compute warps read the stage: TPK threads share a key (each owns 8 rotation
+// pairs, one 16-byte vector from each half of the head dimension), rotate it
+// at its logical position, and keep an online-softmax state (running max,
+// sum, unnormalised output) whose reference max moves lazily.  States are
+// merged across the warp by shuffles, across warps in shared memory, and
+// across slices by a second kernel.
 #include <math.h>
 
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace yr {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+using tc::mbar_arrive;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
+using tc::mbar_wait_drain;
+using tc::smem_u32;
 
-struct OnlineState {
-  float m, l;
+constexpr int kWarps = 8;                    // compute warps
+constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
+constexpr int NSTG = 3;                      // shared-memory stages
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+// PPT rotation pairs per thread: 8 (two 16-byte vectors per key row) when
+// one query head shares the key, 4 when several do, so the per-thread query and
+// accumulator state fits the registers of nine resident warps.
+template <int D, int PPT>
+struct DecodeShape {
+  static constexpr int TPK = D / 2 / PPT;     // threads per key
+  static constexpr int KPW = 32 / TPK;        // keys per warp step
+  static constexpr int KPS = KPW * kWarps;    // keys per CTA step
+  static constexpr int CK = 2 * KPS;          // keys per chunk (2 per thread)
+  static constexpr int ROW = D * 2;           // bytes per cache row
+  static constexpr int STAGE = CK * ROW;      // bytes of K (or V) per stage
+  static constexpr int SMEM = 2 * NSTG * STAGE;
 };
 
 __device__ __forceinline__ float exp2_diff(float a, float b) {
@@ -33,19 +58,46 @@ __device__ __forceinline__ float exp2_diff(float a, float b) {
   return a == -INFINITY ? 0.f : exp2f(a - b);
 }
 
+template <int N>
+__device__ __forceinline__ void load_bf16(const uint8_t* p, float (&x)[N]) {
+  if constexpr (N == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeLaunch a, RopeFreqs f) {
-  constexpr int TPK = D / 16;     // threads per key
-  constexpr int KPW = 32 / TPK;   // keys per warp step
-  constexpr int KPS = KPW * kWarps;
+__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(DecodeLaunch a, RopeFreqs f) {
+  constexpr int PPT = G >= 2 ? 4 : 8;
+  using Sh = DecodeShape<D, PPT>;
+  constexpr int TPK = Sh::TPK, KPW = Sh::KPW, KPS = Sh::KPS, CK = Sh::CK, ROW = Sh::ROW;
   constexpr int HALF = D / 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + NSTG * Sh::STAGE;
+  __shared__ uint64_t full[NSTG], empty[NSTG];
+  __shared__ volatile int abort_flag;
+
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = lane % TPK, kg = lane / TPK;
   const int bh = blockIdx.x;
   const int b = bh / a.Hkv, hkv = bh % a.Hkv;
   const int hq0 = hkv * (a.Hq / a.Hkv) + blockIdx.z * G;
   const int split = blockIdx.y;
   const int C = a.sink + a.window;
+  int* status = a.status;
 
   int n = a.n_valid[b];
   n = n < 0 ? 0 : (n > C ? C : n);
@@ -55,162 +107,208 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeLaunch a, RopeFr
   const int j0 = min(n, split * per);
   const int j1 = min(n, j0 + per);
 
-  float2 fr[8];
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NSTG; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+
+  const uint8_t* kbase = static_cast<const uint8_t*>(a.kc) + (int64_t)bh * C * ROW;
+  const uint8_t* vbase = static_cast<const uint8_t*>(a.vc) + (int64_t)bh * C * ROW;
+
+  if (warp == kWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int issued[NSTG] = {0};
+      int c = 0;
+      for (int jc = j0; jc < j1; jc += CK, ++c) {
+        const int s = c % NSTG;
+        if (!mbar_wait(&empty[s], ((c / NSTG) & 1) ^ 1, &abort_flag, status, 41)) break;
+        const int nk = min(CK, j1 - jc);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nk * ROW));
+        for (int j = jc; j < jc + nk;) {
+          int phys, stop;
+          if (j < a.sink) {
+            phys = j;
+            stop = min(jc + nk, a.sink);
+          } else {
+            const int t = (rs + j - a.sink) % a.window;
+            phys = a.sink + t;
+            stop = min(jc + nk, j + (a.window - t));
+          }
+          const uint32_t bytes = (uint32_t)((stop - j) * ROW);
+          const int off = (j - jc) * ROW;
+          bulk_g2s(sK + s * Sh::STAGE + off, kbase + (int64_t)phys * ROW, bytes, &full[s]);
+          bulk_g2s(sV + s * Sh::STAGE + off, vbase + (int64_t)phys * ROW, bytes, &full[s]);
+          j = stop;
+        }
+        ++issued[s];
+      }
+      if (abort_flag)
+        for (int s = 0; s < NSTG; ++s)
+          if (issued[s]) mbar_wait_drain(&full[s], (issued[s] - 1) & 1, 100000000ull);
+    }
+    __syncwarp();
+    __syncthreads();
+    return;
+  }
+
+  // ---------------- compute warps ----------------
+  const int c8 = lane % TPK, kg = lane / TPK;
+  float2 fr[PPT];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) fr[k] = f.f[c * 8 + k];
+  for (int k = 0; k < PPT; ++k) fr[k] = f.f[c8 * PPT + k];
   const bool identity = f.identity != 0;
 
   // Rotated query at position n - 1, pre-multiplied by scale * log2(e) so
   // that the dot product is the logit in base-2 units.
-  float q1[G][8], q2[G][8];
+  float q1[G][PPT], q2[G][PPT];
   {
-    float cs[8], sn[8];
+    float cs[PPT], sn[PPT];
     const float mq = (float)(n > 0 ? n - 1 : 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < PPT; ++k) {
       if (identity) { cs[k] = 1.f; sn[k] = 0.f; }
       else turn_cos_sin<false>(mq, fr[k], cs[k], sn[k]);
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)b * a.Hq + hq0 + g) * D;
-      const uint4 u1 = *reinterpret_cast<const uint4*>(qp + c * 8);
-      const uint4 u2 = *reinterpret_cast<const uint4*>(qp + HALF + c * 8);
-      const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+      const uint8_t* qp = static_cast<const uint8_t*>(a.q) + ((int64_t)b * a.Hq + hq0 + g) * ROW;
+      float x1[PPT], x2[PPT];
+      load_bf16<PPT>(qp + c8 * PPT * 2, x1);
+      load_bf16<PPT>(qp + HALF * 2 + c8 * PPT * 2, x2);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float x1 = (k & 1) ? bf16_hi(w1[k >> 1]) : bf16_lo(w1[k >> 1]);
-        const float x2 = (k & 1) ? bf16_hi(w2[k >> 1]) : bf16_lo(w2[k >> 1]);
-        q1[g][k] = (x1 * cs[k] - x2 * sn[k]) * a.scale_log2;
-        q2[g][k] = (x1 * sn[k] + x2 * cs[k]) * a.scale_log2;
+      for (int k = 0; k < PPT; ++k) {
+        q1[g][k] = (x1[k] * cs[k] - x2[k] * sn[k]) * a.scale_log2;
+        q2[g][k] = (x1[k] * sn[k] + x2[k] * cs[k]) * a.scale_log2;
       }
     }
   }
 
-  OnlineState st[G];
-  float acc1[G][8], acc2[G][8];
+  float mrun[G], lrun[G], acc1[G][PPT], acc2[G][PPT];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    st[g].m = -INFINITY; st[g].l = 0.f;
+    mrun[g] = -INFINITY;
+    lrun[g] = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) { acc1[g][k] = 0.f; acc2[g][k] = 0.f; }
+    for (int k = 0; k < PPT; ++k) { acc1[g][k] = 0.f; acc2[g][k] = 0.f; }
   }
 
-  const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(a.kc) + (int64_t)bh * C * D + c * 8;
-  const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(a.vc) + (int64_t)bh * C * D + c * 8;
-
-  constexpr int U = 2;  // keys in flight per thread
-  // jw is warp-uniform, so every lane runs the shuffles; lanes past the end
-  // load nothing and skip the update.
-  for (int jw = j0 + warp * KPW; jw < j1; jw += U * KPS) {
-    const int jb = jw + kg;
-    uint4 kd1[U], kd2[U], vd1[U], vd2[U];
-    bool ok[U];
+  bool ok = true;
+  int c = 0;
+  for (int jc = j0; jc < j1; jc += CK, ++c) {
+    const int s = c % NSTG;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (c / NSTG) & 1, &abort_flag, status, 42));
+    if (!ok) break;
+    const uint8_t* stK = sK + s * Sh::STAGE;
+    const uint8_t* stV = sV + s * Sh::STAGE;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = jb + u * KPS;
-      ok[u] = j < j1;
-      if (ok[u]) {
-        int t = j - a.sink;
-        const int phys = j < a.sink ? j : a.sink + ((rs + t) % a.window);
-        const int64_t off = (int64_t)phys * D;
-        kd1[u] = __ldg(reinterpret_cast<const uint4*>(kbase + off));
-        kd2[u] = __ldg(reinterpret_cast<const uint4*>(kbase + off + HALF));
-        vd1[u] = __ldg(reinterpret_cast<const uint4*>(vbase + off));
-        vd2[u] = __ldg(reinterpret_cast<const uint4*>(vbase + off + HALF));
-      } else {
-        kd1[u] = kd2[u] = vd1[u] = vd2[u] = make_uint4(0, 0, 0, 0);
-      }
-    }
+    for (int u = 0; u < CK / KPS; ++u) {
+      const int kk = u * KPS + warp * KPW + kg;  // key within the chunk
+      const int j = jc + kk;
+      const bool valid = j < j1;
+      const uint8_t* kr = stK + kk * ROW + c8 * PPT * 2;
+      const uint8_t* vr = stV + kk * ROW + c8 * PPT * 2;
+      float x1[PPT], x2[PPT], y1[PPT], y2[PPT];
+      load_bf16<PPT>(kr, x1);
+      load_bf16<PPT>(kr + HALF * 2, x2);
+      load_bf16<PPT>(vr, y1);
+      load_bf16<PPT>(vr + HALF * 2, y2);
+      float kr1[PPT], kr2[PPT];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = jb + u * KPS;
-      const uint32_t k1w[4] = {kd1[u].x, kd1[u].y, kd1[u].z, kd1[u].w};
-      const uint32_t k2w[4] = {kd2[u].x, kd2[u].y, kd2[u].z, kd2[u].w};
-      float kr1[8], kr2[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float x1 = (k & 1) ? bf16_hi(k1w[k >> 1]) : bf16_lo(k1w[k >> 1]);
-        const float x2 = (k & 1) ? bf16_hi(k2w[k >> 1]) : bf16_lo(k2w[k >> 1]);
+      for (int k = 0; k < PPT; ++k) {
         float cs = 1.f, sn = 0.f;
         if (!identity) turn_cos_sin<false>((float)j, fr[k], cs, sn);
-        kr1[k] = x1 * cs - x2 * sn;
-        kr2[k] = x1 * sn + x2 * cs;
+        kr1[k] = x1[k] * cs - x2[k] * sn;
+        kr2[k] = x1[k] * sn + x2[k] * cs;
       }
-      const uint32_t v1w[4] = {vd1[u].x, vd1[u].y, vd1[u].z, vd1[u].w};
-      const uint32_t v2w[4] = {vd2[u].x, vd2[u].y, vd2[u].z, vd2[u].w};
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float dot = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) dot = fmaf(q1[g][k], kr1[k], fmaf(q2[g][k], kr2[k], dot));
+        for (int k = 0; k < PPT; ++k) dot = fmaf(q1[g][k], kr1[k], fmaf(q2[g][k], kr2[k], dot));
 #pragma unroll
         for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (ok[u]) {
-          const float mn = fmaxf(st[g].m, dot);
-          const float corr = exp2_diff(st[g].m, mn);
-          const float p = exp2f(dot - mn);
-          st[g].l = st[g].l * corr + p;
-          st[g].m = mn;
+        if (valid) {
+          if (dot > mrun[g] + kRescaleThreshold) {  // lazy: the reference moves rarely
+            const float corr = exp2_diff(mrun[g], dot);
+            lrun[g] *= corr;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float y1 = (k & 1) ? bf16_hi(v1w[k >> 1]) : bf16_lo(v1w[k >> 1]);
-            const float y2 = (k & 1) ? bf16_hi(v2w[k >> 1]) : bf16_lo(v2w[k >> 1]);
-            acc1[g][k] = fmaf(p, y1, acc1[g][k] * corr);
-            acc2[g][k] = fmaf(p, y2, acc2[g][k] * corr);
+            for (int k = 0; k < PPT; ++k) { acc1[g][k] *= corr; acc2[g][k] *= corr; }
+            mrun[g] = dot;
+          }
+          const float pr = exp2f(dot - mrun[g]);
+          lrun[g] += pr;
+#pragma unroll
+          for (int k = 0; k < PPT; ++k) {
+            acc1[g][k] = fmaf(pr, y1[k], acc1[g][k]);
+            acc2[g][k] = fmaf(pr, y2[k], acc2[g][k]);
           }
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 
-  // Merge the key groups of the warp (lanes with equal c).
+  // Merge the key groups of the warp (lanes with equal c8).
 #pragma unroll
   for (int o = TPK; o < 32; o <<= 1) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float om = __shfl_xor_sync(0xffffffffu, st[g].m, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, st[g].l, o);
-      const float mn = fmaxf(st[g].m, om);
-      const float ca = exp2_diff(st[g].m, mn), cb = exp2_diff(om, mn);
-      st[g].l = st[g].l * ca + ol * cb;
+      const float om = __shfl_xor_sync(0xffffffffu, mrun[g], o);
+      const float ol = __shfl_xor_sync(0xffffffffu, lrun[g], o);
+      const float mn = fmaxf(mrun[g], om);
+      const float ca = exp2_diff(mrun[g], mn), cb = exp2_diff(om, mn);
+      lrun[g] = lrun[g] * ca + ol * cb;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < PPT; ++k) {
         const float a1 = __shfl_xor_sync(0xffffffffu, acc1[g][k], o);
         const float a2 = __shfl_xor_sync(0xffffffffu, acc2[g][k], o);
         acc1[g][k] = acc1[g][k] * ca + a1 * cb;
         acc2[g][k] = acc2[g][k] * ca + a2 * cb;
       }
-      st[g].m = mn;
+      mrun[g] = mn;
     }
   }
 
-  // Merge the warps in shared memory.
-  __shared__ float s_acc[kWarps][G][D];
-  __shared__ float s_ml[kWarps][G][2];
+  // Merge the warps in shared memory, reusing the stage buffers: every copy
+  // the producer issued has been consumed (or drained after an abort) once
+  // the block barrier below is passed.
+  __syncthreads();
+  float* s_acc = reinterpret_cast<float*>(smem);           // [kWarps][G][D]
+  float* s_ml = s_acc + kWarps * G * D;                     // [kWarps][G][2]
   if (kg == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        s_acc[warp][g][c * 8 + k] = acc1[g][k];
-        s_acc[warp][g][HALF + c * 8 + k] = acc2[g][k];
+      for (int k = 0; k < PPT; ++k) {
+        s_acc[(warp * G + g) * D + c8 * PPT + k] = acc1[g][k];
+        s_acc[(warp * G + g) * D + HALF + c8 * PPT + k] = acc2[g][k];
       }
-      if (c == 0) { s_ml[warp][g][0] = st[g].m; s_ml[warp][g][1] = st[g].l; }
+      if (c8 == 0) {
+        s_ml[(warp * G + g) * 2 + 0] = mrun[g];
+        s_ml[(warp * G + g) * 2 + 1] = lrun[g];
+      }
     }
   }
-  __syncthreads();
-  for (int t = threadIdx.x; t < G * D; t += kThreads) {
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32));  // compute warps only
+  if (abort_flag) return;
+  for (int t = threadIdx.x; t < G * D; t += kWarps * 32) {
     const int g = t / D, dim = t % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][g][0]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[(w * G + g) * 2]);
     float L = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float wt = exp2_diff(s_ml[w][g][0], M);
-      L += s_ml[w][g][1] * wt;
-      O += s_acc[w][g][dim] * wt;
+      const float wt = exp2_diff(s_ml[(w * G + g) * 2], M);
+      L += s_ml[(w * G + g) * 2 + 1] * wt;
+      O += s_acc[(w * G + g) * D + dim] * wt;
     }
     const int64_t bhq = (int64_t)b * a.Hq + hq0 + g;
     if (a.splits == 1) {
@@ -254,7 +352,10 @@ template <int D, int G>
 cudaError_t launch_dg(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int groups = (a.Hq / a.Hkv) / G;
   dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)a.splits, (unsigned)groups);
-  decode_kernel<D, G><<<grid, kThreads, 0, st>>>(a, f);
+  const int smem = DecodeShape<D, (G >= 2 ? 4 : 8)>::SMEM;
+  cudaError_t e0 = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e0 != cudaSuccess) return e0;
+  decode_kernel<D, G><<<grid, kThreads, smem, st>>>(a, f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   decode_merge_kernel<<<(unsigned)(a.B * a.Hq), 128, 0, st>>>(a);
@@ -263,7 +364,10 @@ cudaError_t launch_dg(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeLaunch& a_in, const RopeFreqs& f, cudaStream_t st) {
+  DecodeLaunch a = a_in;
+  a.status = device_status_word();
+  if (!a.status) return cudaErrorInvalidValue;
   const int G = a.Hq / a.Hkv;
   if (a.d == 128) {
     if (G == 1) return launch_dg<128, 1>(a, f, st);

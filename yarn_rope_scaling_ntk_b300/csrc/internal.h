@@ -60,6 +60,7 @@ struct DecodeLaunch {
   float* ws;  // split partials (NULL when splits == 1)
   int B, Hq, Hkv, d, sink, window, splits;
   float scale_log2;
+  int* status;  // device status word (set by the launcher)
 };
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
