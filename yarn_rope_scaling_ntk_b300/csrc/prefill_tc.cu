@@ -9,18 +9,25 @@
 // sink + window mask ("Context Length Extension", Sliding Window + Attention
 // Sinks).
 //
-// One CTA = one 128-row query tile of one (batch, head).  Roles:
-//   warp 4  TMA producer: Q once, then K and V tiles of 128 keys into a
-//           two-stage ring of 128-byte-swizzled shared-memory buffers.
-//   warp 5  TMEM owner and MMA issuer (one thread): S = Q K^T into one of two
-//           128-column TMEM buffers, then O += P V with P read from TMEM.
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); it reads its
-//           row of S, masks, updates the running max / sum, writes P as
-//           bf16 pairs over the first 64 columns of the same buffer, and
-//           rescales O in TMEM only when the max grew by more than 2^8.
-// The MMA of S for tile i+1 overlaps the softmax of tile i.  Every mbarrier
-// wait is bounded; a wait that gives up records a code in the status word and
-// makes every role leave its loop, drain its asynchronous work and free TMEM.
+// One CTA = two 128-row query tiles (256 consecutive rows) of one (batch,
+// head); both tiles share every key/value tile the CTA loads.  Roles:
+//   warp 9     TMA producer: Q0 and Q1 once, then K and V tiles of 128 keys
+//              into two-stage rings of 128-byte-swizzled shared memory.
+//   warp 8     TMEM owner and MMA issuer (one thread).  For key tile j it
+//              issues, in this order, O0 += P0(j) V(j), S0(j+1) = Q0 K(j+1)^T,
+//              O1 += P1(j) V(j), S1(j+1) = Q1 K(j+1)^T, so that while one
+//              softmax group works on its S the tensor pipe runs the other
+//              group's products (ping-pong).
+//   warps 0-3  softmax group 0 (query tile 0), warps 4-7 group 1 (tile 1):
+//              thread r owns query row r (TMEM lane r).  It reads its row of
+//              S, masks, updates the running max / sum, writes P as bf16
+//              pairs over the first 64 columns of the same TMEM buffer, and
+//              rescales its O rows in TMEM only when the max grew by more
+//              than 2^8 (lazy rescale).  Each group then writes its O / l and
+//              the log-sum-exp.
+// TMEM (512 columns): S0 | S1 | O0 | O1.  Every mbarrier wait is bounded; a
+// wait that gives up records a code in the status word and makes every role
+// leave its loop, drain its asynchronous work and free TMEM.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <string.h>
@@ -34,15 +41,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128;   // query rows per CTA
+constexpr int BM = 128;   // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;   // keys per tile
-constexpr int NS = 2;     // K / V pipeline stages
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct TcParams {
-  int B, Hq, Hkv, S, group;
+  int B, Hq, Hkv, S, group, n_pairs;
   int mask, sink, window, ring_blocks, cs;
   float scale_log2;
   void* o;
@@ -52,13 +60,16 @@ struct TcParams {
   int* status;
 };
 
-// Key chunks in ring order for one query tile: ring blocks I, I-1, ... (then
-// the rest of the ring when nothing is masked), chunks ascending in a block.
-// A chunk holds cs <= 128 keys (cs = 64 when a ring block is an odd multiple
-// of 64 keys); the MMA tile always spans 128 keys and masks the excess.
+// Key chunks in ring order for one CTA (two query tiles): ring blocks I,
+// I-1, ... (I = block of the CTA's last row), chunks ascending in a block.  A
+// chunk holds cs <= 128 keys (cs = 64 when a ring block is an odd multiple of
+// 64 keys); the MMA tile always spans 128 keys and masks the excess.  A chunk
+// is walked when either tile sees part of it; vis[w] says whether tile w does.
 struct Walk {
-  int u, n_chunks, cpb, N, I, cs, S, m0, m1, mask, sink, window;
-  __device__ void init(const TcParams& p, int qt) {
+  int u, n_chunks, cpb, N, I, cs, S, mask, sink, window;
+  int r0[2], r1[2];
+  bool has[2];
+  __device__ void init(const TcParams& p, int pair) {
     u = 0;
     cs = p.cs;
     S = p.S;
@@ -66,30 +77,41 @@ struct Walk {
     N = p.ring_blocks;
     const int bs = N > 1 ? p.S / N : 0;
     cpb = N > 1 ? bs / cs : n_chunks;
-    m0 = qt * BM;
-    m1 = min(p.S, m0 + BM) - 1;
-    I = N > 1 ? m1 / bs : 0;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      r0[w] = pair * 2 * BM + w * BM;
+      has[w] = r0[w] < p.S;
+      r1[w] = min(p.S, r0[w] + BM) - 1;
+    }
+    I = N > 1 ? (has[1] ? r1[1] : r1[0]) / bs : 0;
     mask = p.mask;
     sink = p.sink;
     window = p.window;
   }
-  __device__ bool visible(int n0) const {
-    if (n0 >= S) return false;
+  __device__ bool visible(int w, int n0) const {
+    if (!has[w] || n0 >= S) return false;
     if (mask == YR_MASK_NONE) return true;
-    if (n0 > m1) return false;
-    if (mask == YR_MASK_SINK_WINDOW && n0 >= sink && n0 + cs - 1 <= m0 - window) return false;
+    if (n0 > r1[w]) return false;
+    if (mask == YR_MASK_SINK_WINDOW && n0 >= sink && n0 + cs - 1 <= r0[w] - window) return false;
     return true;
   }
-  // next visible chunk start, or -1
-  __device__ int next() {
+  // next chunk start seen by either tile (or -1), with per-tile visibility
+  __device__ int next(bool& v0, bool& v1) {
     while (u < n_chunks) {
       const int blk = u / cpb;
       const int rb = ((I - blk) % N + N) % N;
       const int n0 = (rb * cpb + (u % cpb)) * cs;
       ++u;
-      if (visible(n0)) return n0;
+      v0 = visible(0, n0);
+      v1 = visible(1, n0);
+      if (v0 || v1) return n0;
     }
     return -1;
+  }
+  // does tile w need the per-element mask on chunk n0?
+  __device__ bool needs_mask(int w, int n0) const {
+    return cs < BN || n0 + BN > S || (mask != YR_MASK_NONE && n0 + BN - 1 > r0[w]) ||
+           (mask == YR_MASK_SINK_WINDOW && n0 <= r1[w] - window);
   }
 };
 
@@ -99,11 +121,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
-struct Smem {
-  static constexpr int kTile = BM * D * 2;  // bytes of one 128-row bf16 tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kTile;
+struct Cfg {
+  static constexpr int NS = D == 128 ? 2 : 4;  // K / V pipeline stages
+  static constexpr int kTile = BM * D * 2;     // bytes of one 128-row bf16 tile
+  static constexpr int kQ = 0;                 // Q0, Q1
+  static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + NS * kTile;
   static constexpr int kBytes = kV + NS * kTile;
 };
@@ -112,8 +141,10 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcParams p) {
-  constexpr int ATOMS = D / 64;              // 64-column swizzle atoms per row
-  constexpr int ATOM_BYTES = BM * 128;       // one atom column of a 128-row tile
+  using C = Cfg<D>;
+  constexpr int NS = C::NS;
+  constexpr int ATOMS = D / 64;         // 64-column swizzle atoms per row
+  constexpr int ATOM_BYTES = BM * 128;  // one atom column of a 128-row tile
   constexpr uint32_t S_COLS = 128;
   constexpr uint32_t O_COL = 2 * S_COLS;
   constexpr uint32_t ID_QK = idesc_bf16_f32(BM, BN, false);
@@ -121,19 +152,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + Smem<D>::kQ;
-  uint8_t* sK = smem + Smem<D>::kK;
-  uint8_t* sV = smem + Smem<D>::kV;
+  uint8_t* sQ = smem + C::kQ;
+  uint8_t* sK = smem + C::kK;
+  uint8_t* sV = smem + C::kV;
 
   __shared__ uint64_t q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  __shared__ uint64_t s_full[2], p_full[2], o_done, drain;
+  __shared__ uint64_t s_full[2], p_full[2], o_done[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_qt = (p.S + BM - 1) / BM;
-  const int qt = n_qt - 1 - (int)blockIdx.x;
-  const int bh = blockIdx.y;
+  // heaviest CTAs first across all heads: the last query-tile pairs of every
+  // (batch, head) come first in launch order
+  const int BH = p.B * p.Hq;
+  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int bh = blockIdx.x % BH;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int hkv = hq / p.group;
 
@@ -146,45 +179,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&s_full[w], 1);
+      mbar_init(&p_full[w], 4);  // one arrival per softmax warp
+      mbar_init(&o_done[w], 1);
     }
-    mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
   Walk walk;
-  walk.init(p, qt);
+  walk.init(p, pair);
 
-  if (warp == 4) {
+  if (warp == kLoadWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&q_full, Smem<D>::kTile);
-      for (int a = 0; a < ATOMS; ++a) tma_load_4d(sQ + a * ATOM_BYTES, &tq, &q_full, a * 64, walk.m0, hq, b);
+      const int nq = walk.has[1] ? 2 : 1;
+      mbar_arrive_expect_tx(&q_full, nq * C::kTile);
+      for (int w = 0; w < nq; ++w)
+        for (int a = 0; a < ATOMS; ++a)
+          tma_load_4d(sQ + w * C::kTile + a * ATOM_BYTES, &tq, &q_full, a * 64, walk.r0[w], hq, b);
       int i = 0;
       int k_uses[NS] = {0}, v_uses[NS] = {0};
-      for (int n0 = walk.next(); n0 >= 0; n0 = walk.next(), ++i) {
+      bool v0, v1;
+      for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1), ++i) {
         const int s = i % NS;
         const uint32_t par = ((i / NS) & 1) ^ 1;
         if (!mbar_wait(&k_empty[s], par, &abort_flag, p.status, 11)) break;
-        mbar_arrive_expect_tx(&k_full[s], Smem<D>::kTile);
+        mbar_arrive_expect_tx(&k_full[s], C::kTile);
         for (int a = 0; a < ATOMS; ++a)
-          tma_load_4d(sK + s * Smem<D>::kTile + a * ATOM_BYTES, &tk, &k_full[s], a * 64, n0, hkv, b);
+          tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &k_full[s], a * 64, n0, hkv, b);
         ++k_uses[s];
         if (!mbar_wait(&v_empty[s], par, &abort_flag, p.status, 12)) break;
-        mbar_arrive_expect_tx(&v_full[s], Smem<D>::kTile);
+        mbar_arrive_expect_tx(&v_full[s], C::kTile);
         for (int a = 0; a < ATOMS; ++a)
-          tma_load_4d(sV + s * Smem<D>::kTile + a * ATOM_BYTES, &tv, &v_full[s], a * 64, n0, hkv, b);
+          tma_load_4d(sV + s * C::kTile + a * ATOM_BYTES, &tv, &v_full[s], a * 64, n0, hkv, b);
         ++v_uses[s];
       }
       if (abort_flag) {
@@ -197,52 +234,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
       const uint32_t q_base = smem_u32(sQ);
-      int i = 0;
-      for (int n0 = ok ? walk.next() : -1; n0 >= 0; n0 = walk.next(), ++i) {
-        const int s = i % NS, sb = i & 1;
-        if (!mbar_wait(&k_full[s], (i / NS) & 1, &abort_flag, p.status, 22)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_base = smem_u32(sK + s * Smem<D>::kTile);
-        const uint32_t d_s = tmem + sb * S_COLS;
+      auto issue_s = [&](int w, int s) {
+        const uint32_t k_base = smem_u32(sK + s * C::kTile);
+        const uint32_t qb = q_base + w * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * ATOM_BYTES + (kk & 3) * 32;
-          mma_ss(d_s, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), ID_QK, kk > 0);
+          mma_ss(tmem + w * S_COLS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), ID_QK,
+                 kk > 0);
         }
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[s]);
-        if (i > 0) {
-          const int j = i - 1, sj = j % NS, pb = j & 1;
-          if (!mbar_wait(&p_full[pb], (j >> 1) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
-          if (!mbar_wait(&v_full[sj], (j / NS) & 1, &abort_flag, p.status, 24)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(sV + sj * Smem<D>::kTile);
+        mma_commit(&s_full[w]);
+      };
+      auto issue_pv = [&](int w, int s, bool acc) {
+        const uint32_t v_base = smem_u32(sV + s * C::kTile);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + O_COL, tmem + pb * S_COLS + kk * 8, sdesc_sw128(v_base + kk * 2048, ATOM_BYTES, 1024),
-                   ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&v_empty[sj]);
-          mma_commit(&o_done);
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + O_COL + w * D, tmem + w * S_COLS + kk * 8,
+                 sdesc_sw128(v_base + kk * 2048, ATOM_BYTES, 1024), ID_PV, (acc || kk > 0) ? 1u : 0u);
+        mma_commit(&o_done[w]);
+      };
+      bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
+      int pv_count[2] = {0, 0};
+      // chunk i: (n0, v0, v1); the S products of chunk i are issued before
+      // the PV products of chunk i - 1
+      bool cv0 = false, cv1 = false;
+      int cur = ok ? walk.next(cv0, cv1) : -1;
+      int i = 0;
+      if (cur >= 0) {
+        ok = mbar_wait(&k_full[0], 0, &abort_flag, p.status, 22);
+        if (ok) {
+          tc_fence_after();
+          if (cv0) issue_s(0, 0);
+          if (cv1) issue_s(1, 0);
+          mma_commit(&k_empty[0]);
         }
       }
-      if (ok && i > 0) {
-        const int j = i - 1, sj = j % NS, pb = j & 1;
-        if (mbar_wait(&p_full[pb], (j >> 1) & 1, &abort_flag, p.status, 25) &&
-            mbar_wait(&v_full[sj], (j / NS) & 1, &abort_flag, p.status, 26)) {
+      while (ok && cur >= 0) {
+        const int s = i % NS;
+        bool nv0 = false, nv1 = false;
+        const int nxt = walk.next(nv0, nv1);
+        const int sn = (i + 1) % NS;
+        if (!mbar_wait(&v_full[s], (i / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
+        if (cv0) {
+          if (!mbar_wait(&p_full[0], pv_count[0] & 1, &abort_flag, p.status, 25)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t v_base = smem_u32(sV + sj * Smem<D>::kTile);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + O_COL, tmem + pb * S_COLS + kk * 8, sdesc_sw128(v_base + kk * 2048, ATOM_BYTES, 1024),
-                   ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&v_empty[sj]);
-          mma_commit(&o_done);
+          issue_pv(0, s, pv_count[0] > 0);
+          ++pv_count[0];
         }
+        if (nxt >= 0 && !mbar_wait(&k_full[sn], ((i + 1) / NS) & 1, &abort_flag, p.status, 24)) {
+          ok = false;
+          break;
+        }
+        if (nxt >= 0 && nv0) {
+          tc_fence_after();
+          issue_s(0, sn);
+        }
+        if (cv1) {
+          if (!mbar_wait(&p_full[1], pv_count[1] & 1, &abort_flag, p.status, 26)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(1, s, pv_count[1] > 0);
+          ++pv_count[1];
+        }
+        if (nxt >= 0) {
+          if (nv1) {
+            tc_fence_after();
+            issue_s(1, sn);
+          }
+          mma_commit(&k_empty[sn]);
+        }
+        mma_commit(&v_empty[s]);
+        cur = nxt;
+        cv0 = nv0;
+        cv1 = nv1;
+        ++i;
       }
       // all issued MMAs complete before TMEM is released
       mma_commit(&drain);
@@ -250,31 +318,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- softmax (warps 0-3) ----------------
-    const int r = tid;  // query row within the tile == TMEM lane
-    const int m = walk.m0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    // ---------------- softmax (warps 0-3: tile 0, warps 4-7: tile 1) --------
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // query row within the tile == TMEM lane
+    const int m = walk.r0[wg] + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_addr + wg * S_COLS;
+    const uint32_t o_addr = lane_addr + O_COL + wg * D;
+    const float sc = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     int i = 0;
     bool ok = true;
-    for (int n0 = walk.next(); n0 >= 0; n0 = walk.next(), ++i) {
-      const int sb = i & 1;
+    bool v0, v1;
+    for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1)) {
+      if (!(wg ? v1 : v0)) continue;
       // warp-uniform decisions: tcgen05.ld / st are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, &abort_flag, p.status, 31));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], i & 1, &abort_flag, p.status, 31));
       if (!ok) break;
       tc_fence_after();
+      uint32_t raw[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, raw[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(raw[c]);
       float x[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + sb * S_COLS + c * 32, rr);
-        tmem_ld_wait();
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]) * p.scale_log2;
-      }
-      const bool need_mask = walk.cs < BN || n0 + BN > p.S || (p.mask != YR_MASK_NONE && n0 + BN - 1 > walk.m0) ||
-                             (p.mask == YR_MASK_SINK_WINDOW && n0 <= walk.m1 - p.window);
-      if (need_mask) {
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
+      if (walk.needs_mask(wg, n0)) {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
           const int n = n0 + e;
@@ -286,53 +359,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!vis) x[e] = -INFINITY;
         }
       }
-      float mx = x[0];
+      // row max of the raw logits: eight independent 3-input chains
+      float mx8[8];
 #pragma unroll
-      for (int e = 1; e < BN; ++e) mx = fmaxf(mx, x[e]);
-      // Lazy rescale: the reference max moves only when the row max exceeds it
-      // by more than 2^8; the whole warp rescales its O rows when any lane must.
+      for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+#pragma unroll
+      for (int e = 8; e + 16 <= BN; e += 16)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = max3(mx8[t], x[e + 2 * t], x[e + 2 * t + 1]);
+      // the loop above covers x[8, 120); fold the last 8 in
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], x[BN - 8 + t]);
+      const float mx_raw = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      const float mx = mx_raw * sc;  // -inf stays -inf (sc > 0)
+      // Lazy rescale: the reference max moves only when the row max exceeds
+      // it by more than 2^8.  P is formed against the new reference; the O
+      // rows are rescaled after P is stored (the logits are dead by then),
+      // by the whole warp when any lane must.
       const bool grow = mx > m_used + kRescaleThreshold;
       const bool rescale = grow && m_used != -INFINITY && i > 0;
       const float corr = rescale ? ex2(m_used - mx) : 1.0f;
       if (grow) m_used = mx;
-      if (__any_sync(0xffffffffu, rescale)) {
-        l *= corr;
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done, (i - 1) & 1, &abort_flag, p.status, 32));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(lane_addr + O_COL + c * 32, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-          tmem_st32(lane_addr + O_COL + c * 32, rr);
-        }
-      }
-      const float ref = m_used == -INFINITY ? 0.f : m_used;
-      float sum = 0.f;
+      const float neg_ref = m_used == -INFINITY ? 0.f : -m_used;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float a0 = ex2(x[c * 64 + 2 * e] - ref);
-          const float a1 = ex2(x[c * 64 + 2 * e + 1] - ref);
-          sum += a0 + a1;
+          const float a0 = ex2(fmaf(x[c * 64 + 2 * e], sc, neg_ref));
+          const float a1 = ex2(fmaf(x[c * 64 + 2 * e + 1], sc, neg_ref));
+          sum4[e & 3] += a0 + a1;
           pk[e] = pack_bf16(a0, a1);
         }
-        tmem_st32(lane_addr + sb * S_COLS + c * 32, pk);
+        tmem_st32(s_addr + c * 32, pk);
       }
-      l += sum;
+      l = l * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      if (__any_sync(0xffffffffu, rescale)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (i - 1) & 1, &abort_flag, p.status, 32));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(o_addr + c * 32, rr);
+          tmem_ld_wait();
+          reg_fence32(rr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+          tmem_st32(o_addr + c * 32, rr);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[wg]);
+      ++i;
     }
     // epilogue: O / l -> global, lse
     if (__all_sync(0xffffffffu, ok && !abort_flag)) {
       bool have = true;
-      if (i > 0) have = __all_sync(0xffffffffu, mbar_wait(&o_done, (i - 1) & 1, &abort_flag, p.status, 33));
+      if (i > 0) have = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (i - 1) & 1, &abort_flag, p.status, 33));
       tc_fence_after();
       if (have) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -343,8 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           if (i > 0) {
-            tmem_ld32(lane_addr + O_COL + c * 32, rr);
+            tmem_ld32(o_addr + c * 32, rr);
             tmem_ld_wait();
+            reg_fence32(rr);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) rr[e] = 0u;
@@ -378,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -422,6 +510,7 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.S = a.S; p.group = a.Hq / a.Hkv;
+  p.n_pairs = (a.S + 2 * BM - 1) / (2 * BM);
   p.mask = a.mask; p.sink = a.sink; p.window = a.window; p.ring_blocks = a.ring_blocks;
   p.cs = (a.ring_blocks > 1 && (a.S / a.ring_blocks) % BN != 0) ? 64 : BN;
   p.scale_log2 = a.scale_log2;
@@ -431,11 +520,12 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   p.out_bf16 = a.out_bf16;
   p.status = device_status_word();
   if (!p.status) return cudaErrorInvalidValue;
-  const int smem = Smem<D>::kBytes + 1024;
+  const int smem = Cfg<D>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((a.S + BM - 1) / BM), (unsigned)(a.B * a.Hq));
-  prefill_tc_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
+  const int64_t blocks = (int64_t)p.n_pairs * a.B * a.Hq;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  prefill_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
