@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       }
       if (abort_flag)
         for (int s = 0; s < NSTG; ++s)
-          if (issued[s]) mbar_wait_drain(&full[s], (issued[s] - 1) & 1, 100000000ull);
+          if (issued[s]) mbar_wait_drain(&full[s], (issued[s] - 1) & 1, 200000000ll);
     }
     __syncwarp();
     __syncthreads();

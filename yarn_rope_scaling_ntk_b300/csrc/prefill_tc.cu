@@ -18,6 +18,7 @@
 //              O1 += P1(j) V(j), S1(j+1) = Q1 K(j+1)^T, so that while one
 //              softmax group works on its S the tensor pipe runs the other
 //              group's products (ping-pong).
+//   warps 10-11 idle: their registers go to the softmax groups.
 //   warps 0-3  softmax group 0 (query tile 0), warps 4-7 group 1 (tile 1):
 //              thread r owns query row r (TMEM lane r).  It reads its row of
 //              S, masks, updates the running max / sum, writes P as bf16
@@ -43,9 +44,15 @@ using namespace tc;
 
 constexpr int BM = 128;   // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;   // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;              // 3 warpgroups
 constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kLoadWarp = 9;               // warps 10 and 11 only lend registers
+// Register budgets (launch: 384 threads x 168).  The softmax groups hold a
+// full 128-column row of S in registers; the control warpgroup keeps the
+// MMA issue loop in registers: 2 x 128 x 192 + 128 x 120 = 64512 = 384 x 168.
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsControl = 120;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -60,60 +67,72 @@ struct TcParams {
   int* status;
 };
 
-// Key chunks in ring order for one CTA (two query tiles): ring blocks I,
-// I-1, ... (I = block of the CTA's last row), chunks ascending in a block.  A
-// chunk holds cs <= 128 keys (cs = 64 when a ring block is an odd multiple of
-// 64 keys); the MMA tile always spans 128 keys and masks the excess.  A chunk
-// is walked when either tile sees part of it; vis[w] says whether tile w does.
+// Key chunks in ring order for one CTA (two query tiles a and b): ring
+// blocks I, I-1, ... (I = block of the CTA's last row), chunks ascending in a
+// block.  A chunk holds cs <= 128 keys (cs = 64 when a ring block is an odd
+// multiple of 64 keys); the MMA tile always spans 128 keys and masks the
+// excess.  A chunk is walked when either tile sees part of it; v0 / v1 say
+// which tiles do.  The walk keeps running counters (no division) and leaves a
+// block as soon as its chunks lie past every row of the CTA.
 struct Walk {
-  int u, n_chunks, cpb, N, I, cs, S, mask, sink, window;
-  int r0[2], r1[2];
-  bool has[2];
+  int N, cpb, cs, S, mask, sink, window;
+  int t, c, rb;                // ring step, chunk within the block, block
+  int r0a, r1a, r0b, r1b, lim;
+  bool hasa, hasb;
   __device__ void init(const TcParams& p, int pair) {
-    u = 0;
     cs = p.cs;
     S = p.S;
-    n_chunks = (p.S + cs - 1) / cs;
     N = p.ring_blocks;
+    const int n_chunks = (p.S + cs - 1) / cs;
     const int bs = N > 1 ? p.S / N : 0;
     cpb = N > 1 ? bs / cs : n_chunks;
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      r0[w] = pair * 2 * BM + w * BM;
-      has[w] = r0[w] < p.S;
-      r1[w] = min(p.S, r0[w] + BM) - 1;
-    }
-    I = N > 1 ? (has[1] ? r1[1] : r1[0]) / bs : 0;
+    r0a = pair * 2 * BM;
+    r0b = r0a + BM;
+    hasa = r0a < p.S;
+    hasb = r0b < p.S;
+    r1a = min(p.S, r0a + BM) - 1;
+    r1b = min(p.S, r0b + BM) - 1;
+    lim = hasb ? r1b : r1a;
     mask = p.mask;
     sink = p.sink;
     window = p.window;
+    t = 0;
+    c = 0;
+    rb = N > 1 ? lim / bs : 0;
   }
-  __device__ bool visible(int w, int n0) const {
-    if (!has[w] || n0 >= S) return false;
+  __device__ __forceinline__ bool visible(bool has, int r0, int r1, int n0) const {
+    if (!has) return false;
     if (mask == YR_MASK_NONE) return true;
-    if (n0 > r1[w]) return false;
-    if (mask == YR_MASK_SINK_WINDOW && n0 >= sink && n0 + cs - 1 <= r0[w] - window) return false;
+    if (n0 > r1) return false;
+    if (mask == YR_MASK_SINK_WINDOW && n0 >= sink && n0 + cs - 1 <= r0 - window) return false;
     return true;
   }
   // next chunk start seen by either tile (or -1), with per-tile visibility
   __device__ int next(bool& v0, bool& v1) {
-    while (u < n_chunks) {
-      const int blk = u / cpb;
-      const int rb = ((I - blk) % N + N) % N;
-      const int n0 = (rb * cpb + (u % cpb)) * cs;
-      ++u;
-      v0 = visible(0, n0);
-      v1 = visible(1, n0);
+    while (true) {
+      if (c >= cpb) {
+        if (++t >= N) return -1;
+        rb = rb == 0 ? N - 1 : rb - 1;
+        c = 0;
+      }
+      const int n0 = (rb * cpb + c) * cs;
+      ++c;
+      if (n0 >= S || (mask != YR_MASK_NONE && n0 > lim)) {  // the rest of this block too
+        c = cpb;
+        continue;
+      }
+      v0 = visible(hasa, r0a, r1a, n0);
+      v1 = visible(hasb, r0b, r1b, n0);
       if (v0 || v1) return n0;
     }
-    return -1;
-  }
-  // does tile w need the per-element mask on chunk n0?
-  __device__ bool needs_mask(int w, int n0) const {
-    return cs < BN || n0 + BN > S || (mask != YR_MASK_NONE && n0 + BN - 1 > r0[w]) ||
-           (mask == YR_MASK_SINK_WINDOW && n0 <= r1[w] - window);
   }
 };
+
+// does a tile with rows [r0, r1] need the per-element mask on chunk n0?
+__device__ __forceinline__ bool needs_mask(const TcParams& p, int r0, int r1, int n0) {
+  return p.cs < BN || n0 + BN > p.S || (p.mask != YR_MASK_NONE && n0 + BN - 1 > r0) ||
+         (p.mask == YR_MASK_SINK_WINDOW && n0 <= r1 - p.window);
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -196,132 +215,142 @@ __global__ void __launch_bounds__(kThreads, 1)
   Walk walk;
   walk.init(p, pair);
 
-  if (warp == kLoadWarp) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      const int nq = walk.has[1] ? 2 : 1;
-      mbar_arrive_expect_tx(&q_full, nq * C::kTile);
-      for (int w = 0; w < nq; ++w)
-        for (int a = 0; a < ATOMS; ++a)
-          tma_load_4d(sQ + w * C::kTile + a * ATOM_BYTES, &tq, &q_full, a * 64, walk.r0[w], hq, b);
-      int i = 0;
-      int k_uses[NS] = {0}, v_uses[NS] = {0};
-      bool v0, v1;
-      for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1), ++i) {
-        const int s = i % NS;
-        const uint32_t par = ((i / NS) & 1) ^ 1;
-        if (!mbar_wait(&k_empty[s], par, &abort_flag, p.status, 11)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::kTile);
-        for (int a = 0; a < ATOMS; ++a)
-          tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &k_full[s], a * 64, n0, hkv, b);
-        ++k_uses[s];
-        if (!mbar_wait(&v_empty[s], par, &abort_flag, p.status, 12)) break;
-        mbar_arrive_expect_tx(&v_full[s], C::kTile);
-        for (int a = 0; a < ATOMS; ++a)
-          tma_load_4d(sV + s * C::kTile + a * ATOM_BYTES, &tv, &v_full[s], a * 64, n0, hkv, b);
-        ++v_uses[s];
-      }
-      if (abort_flag) {
-        // let the copies already issued land before the CTA exits
-        mbar_wait_drain(&q_full, 0, 100000000ull);
-        for (int s = 0; s < NS; ++s) {
-          if (k_uses[s]) mbar_wait_drain(&k_full[s], (k_uses[s] - 1) & 1, 100000000ull);
-          if (v_uses[s]) mbar_wait_drain(&v_full[s], (v_uses[s] - 1) & 1, 100000000ull);
+  if (warp >= 8) {
+    reg_dealloc<kRegsControl>();
+    if (warp == kLoadWarp) {
+      // ---------------- TMA producer ----------------
+      if (lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        const int nq = walk.hasb ? 2 : 1;
+        mbar_arrive_expect_tx(&q_full, nq * C::kTile);
+        for (int w = 0; w < nq; ++w)
+          for (int a = 0; a < ATOMS; ++a)
+            tma_load_4d(sQ + w * C::kTile + a * ATOM_BYTES, &tq, &q_full, a * 64, w ? walk.r0b : walk.r0a, hq, b);
+        int i = 0;
+        int k_uses[NS] = {0}, v_uses[NS] = {0};
+        bool v0, v1;
+        for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1), ++i) {
+          const int s = i % NS;
+          const uint32_t par = ((i / NS) & 1) ^ 1;
+          if (!mbar_wait(&k_empty[s], par, &abort_flag, p.status, 11)) break;
+          mbar_arrive_expect_tx(&k_full[s], C::kTile);
+          for (int a = 0; a < ATOMS; ++a)
+            tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &k_full[s], a * 64, n0, hkv, b);
+          ++k_uses[s];
+          if (!mbar_wait(&v_empty[s], par, &abort_flag, p.status, 12)) break;
+          mbar_arrive_expect_tx(&v_full[s], C::kTile);
+          for (int a = 0; a < ATOMS; ++a)
+            tma_load_4d(sV + s * C::kTile + a * ATOM_BYTES, &tv, &v_full[s], a * 64, n0, hkv, b);
+          ++v_uses[s];
         }
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t q_base = smem_u32(sQ);
-      auto issue_s = [&](int w, int s) {
-        const uint32_t k_base = smem_u32(sK + s * C::kTile);
-        const uint32_t qb = q_base + w * C::kTile;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * ATOM_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + w * S_COLS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), ID_QK,
-                 kk > 0);
-        }
-        mma_commit(&s_full[w]);
-      };
-      auto issue_pv = [&](int w, int s, bool acc) {
-        const uint32_t v_base = smem_u32(sV + s * C::kTile);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + O_COL + w * D, tmem + w * S_COLS + kk * 8,
-                 sdesc_sw128(v_base + kk * 2048, ATOM_BYTES, 1024), ID_PV, (acc || kk > 0) ? 1u : 0u);
-        mma_commit(&o_done[w]);
-      };
-      bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
-      int pv_count[2] = {0, 0};
-      // chunk i: (n0, v0, v1); the S products of chunk i are issued before
-      // the PV products of chunk i - 1
-      bool cv0 = false, cv1 = false;
-      int cur = ok ? walk.next(cv0, cv1) : -1;
-      int i = 0;
-      if (cur >= 0) {
-        ok = mbar_wait(&k_full[0], 0, &abort_flag, p.status, 22);
-        if (ok) {
-          tc_fence_after();
-          if (cv0) issue_s(0, 0);
-          if (cv1) issue_s(1, 0);
-          mma_commit(&k_empty[0]);
-        }
-      }
-      while (ok && cur >= 0) {
-        const int s = i % NS;
-        bool nv0 = false, nv1 = false;
-        const int nxt = walk.next(nv0, nv1);
-        const int sn = (i + 1) % NS;
-        if (!mbar_wait(&v_full[s], (i / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
-        if (cv0) {
-          if (!mbar_wait(&p_full[0], pv_count[0] & 1, &abort_flag, p.status, 25)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(0, s, pv_count[0] > 0);
-          ++pv_count[0];
-        }
-        if (nxt >= 0 && !mbar_wait(&k_full[sn], ((i + 1) / NS) & 1, &abort_flag, p.status, 24)) {
-          ok = false;
-          break;
-        }
-        if (nxt >= 0 && nv0) {
-          tc_fence_after();
-          issue_s(0, sn);
-        }
-        if (cv1) {
-          if (!mbar_wait(&p_full[1], pv_count[1] & 1, &abort_flag, p.status, 26)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(1, s, pv_count[1] > 0);
-          ++pv_count[1];
-        }
-        if (nxt >= 0) {
-          if (nv1) {
-            tc_fence_after();
-            issue_s(1, sn);
+        if (abort_flag) {
+          // let the copies already issued land before the CTA exits
+          mbar_wait_drain(&q_full, 0, 200000000ll);
+          for (int s = 0; s < NS; ++s) {
+            if (k_uses[s]) mbar_wait_drain(&k_full[s], (k_uses[s] - 1) & 1, 200000000ll);
+            if (v_uses[s]) mbar_wait_drain(&v_full[s], (v_uses[s] - 1) & 1, 200000000ll);
           }
-          mma_commit(&k_empty[sn]);
         }
-        mma_commit(&v_empty[s]);
-        cur = nxt;
-        cv0 = nv0;
-        cv1 = nv1;
-        ++i;
       }
-      // all issued MMAs complete before TMEM is released
-      mma_commit(&drain);
-      mbar_wait_drain(&drain, 0, 100000000ull);
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ---------------- MMA issuer ----------------
+      if (lane == 0) {
+        // Shared-memory descriptors of every operand buffer, built once; a
+        // K step adds its (compile-time) byte offset / 16 to the start
+        // address field, which cannot carry out (shared addresses < 256 KB).
+        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dv = sdesc_sw128(smem_u32(sV), ATOM_BYTES, 1024);
+        constexpr uint64_t kTile16 = C::kTile >> 4;
+        auto issue_s = [&](int w, int s) {
+          const uint64_t a0 = dq + (w ? kTile16 : 0), b0 = dk + (uint64_t)s * kTile16;
+          const uint32_t d_s = tmem + w * S_COLS;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+            mma_ss(d_s, a0 + off, b0 + off, ID_QK, kk > 0);
+          }
+          mma_commit(&s_full[w]);
+        };
+        auto issue_pv = [&](int w, int s, bool acc) {
+          const uint64_t b0 = dv + (uint64_t)s * kTile16;
+          const uint32_t d_o = tmem + O_COL + w * D, a_p = tmem + w * S_COLS;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(d_o, a_p + kk * 8, b0 + (uint64_t)(kk * 2048 >> 4), ID_PV, (acc || kk > 0) ? 1u : 0u);
+          mma_commit(&o_done[w]);
+        };
+        bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
+        int pv_count[2] = {0, 0};
+        // chunk i: (n0, v0, v1); the S products of chunk i are issued before
+        // the PV products of chunk i - 1
+        bool cv0 = false, cv1 = false;
+        int cur = ok ? walk.next(cv0, cv1) : -1;
+        int i = 0;
+        if (cur >= 0) {
+          ok = mbar_wait(&k_full[0], 0, &abort_flag, p.status, 22);
+          if (ok) {
+            tc_fence_after();
+            if (cv0) issue_s(0, 0);
+            if (cv1) issue_s(1, 0);
+            mma_commit(&k_empty[0]);
+          }
+        }
+        while (ok && cur >= 0) {
+          const int s = i % NS;
+          bool nv0 = false, nv1 = false;
+          const int nxt = walk.next(nv0, nv1);
+          const int sn = (i + 1) % NS;
+          if (!mbar_wait(&v_full[s], (i / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
+          if (cv0) {
+            if (!mbar_wait(&p_full[0], pv_count[0] & 1, &abort_flag, p.status, 25)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(0, s, pv_count[0] > 0);
+            ++pv_count[0];
+          }
+          if (nxt >= 0 && !mbar_wait(&k_full[sn], ((i + 1) / NS) & 1, &abort_flag, p.status, 24)) {
+            ok = false;
+            break;
+          }
+          if (nxt >= 0 && nv0) {
+            tc_fence_after();
+            issue_s(0, sn);
+          }
+          if (cv1) {
+            if (!mbar_wait(&p_full[1], pv_count[1] & 1, &abort_flag, p.status, 26)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(1, s, pv_count[1] > 0);
+            ++pv_count[1];
+          }
+          if (nxt >= 0) {
+            if (nv1) {
+              tc_fence_after();
+              issue_s(1, sn);
+            }
+            mma_commit(&k_empty[sn]);
+          }
+          mma_commit(&v_empty[s]);
+          cur = nxt;
+          cv0 = nv0;
+          cv1 = nv1;
+          ++i;
+        }
+        // all issued MMAs complete before TMEM is released
+        mma_commit(&drain);
+        mbar_wait_drain(&drain, 0, 200000000ll);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    reg_alloc<kRegsSoftmax>();
     // ---------------- softmax (warps 0-3: tile 0, warps 4-7: tile 1) --------
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // query row within the tile == TMEM lane
-    const int m = walk.r0[wg] + r;
+    const int my_r0 = wg ? walk.r0b : walk.r0a, my_r1 = wg ? walk.r1b : walk.r1a;
+    const int m = my_r0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_addr + wg * S_COLS;
     const uint32_t o_addr = lane_addr + O_COL + wg * D;
@@ -347,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
-      if (walk.needs_mask(wg, n0)) {
+      if (needs_mask(p, my_r0, my_r1, n0)) {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
           const int n = n0 + e;
-          bool vis = e < walk.cs && n < p.S;
+          bool vis = e < p.cs && n < p.S;
           if (p.mask != YR_MASK_NONE) {
             vis = vis && n <= m;
             if (p.mask == YR_MASK_SINK_WINDOW) vis = vis && (n < p.sink || m - n < p.window);

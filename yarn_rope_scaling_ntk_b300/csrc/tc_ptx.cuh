@@ -15,12 +15,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -45,16 +39,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity.  Gives up after
-// `limit_ns` or when another role raised `abort`; returns false then.
+// Wait for the phase of `bar` with the given parity.  Gives up after about
+// `limit_cycles` SM clock cycles (4e9: about 2 s at the 2 GHz maximum clock)
+// or when another role raised `abort`; returns false then.  The bound uses
+// the SM cycle counter, which is cheap to read, so a completed phase is seen
+// within a few cycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status, int code, uint64_t limit_ns = 2000000000ull) {
+                                          int* status, int code, long long limit_cycles = 4000000000ll) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if (clock64() - t0 > limit_cycles) {
       atomicCAS(status, 0, code);
       *abort = 1;
       return false;
@@ -64,11 +61,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Bounded wait that ignores the abort flag: used to drain a CTA's own
 // asynchronous copies and MMAs before it releases its resources.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   return true;
 }
 
@@ -144,6 +141,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&r)[32]
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- per-warpgroup register budgets ---------------------------------------
+// setmaxnreg moves registers between the warpgroups of a CTA; all four warps
+// of a warpgroup execute it.  The budgets of all warpgroups must add up to at
+// most the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---- tcgen05 MMA ------------------------------------------------------------
 // Shared-memory matrix descriptor: start address, leading- and stride-
