@@ -72,16 +72,17 @@ struct TcParams {
 // block.  A chunk holds cs <= 128 keys (cs = 64 when a ring block is an odd
 // multiple of 64 keys); the MMA tile always spans 128 keys and masks the
 // excess.  A chunk is walked when either tile sees part of it; v0 / v1 say
-// which tiles do.  The walk keeps running counters (no division) and leaves a
-// block as soon as its chunks lie past every row of the CTA.
+// which tiles do.  Under a mask the chunks any row of the CTA can see form the
+// range [0, last] minus at most one gap [gap_lo, gap_hi) (chunks between the
+// sinks and the start of the window), so the walk is a few compares per chunk.
 struct Walk {
-  int N, cpb, cs, S, mask, sink, window;
-  int t, c, rb;                // ring step, chunk within the block, block
-  int r0a, r1a, r0b, r1b, lim;
+  int N, cpb, cs, mask, sink, window;
+  int r0a, r1a, r0b, r1b;
   bool hasa, hasb;
+  int last, gap_lo, gap_hi, I;
+  int t, c, c_end, rb;  // ring step, chunk, end of the block's visible chunks, block
   __device__ void init(const TcParams& p, int pair) {
     cs = p.cs;
-    S = p.S;
     N = p.ring_blocks;
     const int n_chunks = (p.S + cs - 1) / cs;
     const int bs = N > 1 ? p.S / N : 0;
@@ -92,38 +93,48 @@ struct Walk {
     hasb = r0b < p.S;
     r1a = min(p.S, r0a + BM) - 1;
     r1b = min(p.S, r0b + BM) - 1;
-    lim = hasb ? r1b : r1a;
+    const int lim = hasb ? r1b : r1a;
     mask = p.mask;
     sink = p.sink;
     window = p.window;
-    t = 0;
-    c = 0;
-    rb = N > 1 ? lim / bs : 0;
+    last = mask == YR_MASK_NONE ? n_chunks - 1 : min(n_chunks - 1, lim / cs);
+    gap_lo = gap_hi = 0;
+    if (mask == YR_MASK_SINK_WINDOW) {
+      // chunks with a sink: c * cs < sink; chunks that reach the window of
+      // row r0a: c * cs + cs - 1 > r0a - window
+      const int sink_chunks = (sink + cs - 1) / cs;
+      const int x = r0a - window - cs + 1;
+      const int w_lo = x < 0 ? 0 : x / cs + 1;
+      if (sink_chunks < w_lo) { gap_lo = sink_chunks; gap_hi = w_lo; }
+    }
+    I = N > 1 ? lim / bs : 0;
+    t = -1;
+    c = c_end = 0;
+    rb = 0;
   }
   __device__ __forceinline__ bool visible(bool has, int r0, int r1, int n0) const {
-    if (!has) return false;
-    if (mask == YR_MASK_NONE) return true;
-    if (n0 > r1) return false;
-    if (mask == YR_MASK_SINK_WINDOW && n0 >= sink && n0 + cs - 1 <= r0 - window) return false;
-    return true;
+    const bool in_window = (mask != YR_MASK_SINK_WINDOW) | (n0 < sink) | (n0 + cs - 1 > r0 - window);
+    return has & ((mask == YR_MASK_NONE) | ((n0 <= r1) & in_window));
   }
   // next chunk start seen by either tile (or -1), with per-tile visibility
-  __device__ int next(bool& v0, bool& v1) {
+  __device__ __forceinline__ int next(bool& v0, bool& v1) {
     while (true) {
-      if (c >= cpb) {
+      if (c >= c_end) {
         if (++t >= N) return -1;
-        rb = rb == 0 ? N - 1 : rb - 1;
-        c = 0;
-      }
-      const int n0 = (rb * cpb + c) * cs;
-      ++c;
-      if (n0 >= S || (mask != YR_MASK_NONE && n0 > lim)) {  // the rest of this block too
-        c = cpb;
+        rb = t == 0 ? I : (rb == 0 ? N - 1 : rb - 1);
+        c = rb * cpb;
+        c_end = min(c + cpb, last + 1);
         continue;
       }
+      if (c >= gap_lo && c < gap_hi) {
+        c = gap_hi;
+        continue;
+      }
+      const int n0 = c * cs;
+      ++c;
       v0 = visible(hasa, r0a, r1a, n0);
       v1 = visible(hasb, r0b, r1b, n0);
-      if (v0 || v1) return n0;
+      if (v0 | v1) return n0;
     }
   }
 };
@@ -175,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + C::kK;
   uint8_t* sV = smem + C::kV;
 
-  __shared__ uint64_t q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  __shared__ uint64_t q_full, kv_full[NS], kv_empty[NS];
   __shared__ uint64_t s_full[2], p_full[2], o_done[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -193,10 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     mbar_init(&q_full, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&s_full[w], 1);
@@ -228,30 +237,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < nq; ++w)
           for (int a = 0; a < ATOMS; ++a)
             tma_load_4d(sQ + w * C::kTile + a * ATOM_BYTES, &tq, &q_full, a * 64, w ? walk.r0b : walk.r0a, hq, b);
-        int i = 0;
-        int k_uses[NS] = {0}, v_uses[NS] = {0};
+        // Load unit u: K(0) for u = 0; V(u-1) and (when chunk u exists) K(u)
+        // otherwise, on barrier u % NS.  K(c) lives in K buffer c % NS and
+        // V(c) in V buffer c % NS, so unit u reuses exactly the buffers of
+        // unit u - NS and waits for that unit's release.
+        int uses[NS] = {0};
         bool v0, v1;
-        for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1), ++i) {
-          const int s = i % NS;
-          const uint32_t par = ((i / NS) & 1) ^ 1;
-          if (!mbar_wait(&k_empty[s], par, &abort_flag, p.status, 11)) break;
-          mbar_arrive_expect_tx(&k_full[s], C::kTile);
-          for (int a = 0; a < ATOMS; ++a)
-            tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &k_full[s], a * 64, n0, hkv, b);
-          ++k_uses[s];
-          if (!mbar_wait(&v_empty[s], par, &abort_flag, p.status, 12)) break;
-          mbar_arrive_expect_tx(&v_full[s], C::kTile);
-          for (int a = 0; a < ATOMS; ++a)
-            tma_load_4d(sV + s * C::kTile + a * ATOM_BYTES, &tv, &v_full[s], a * 64, n0, hkv, b);
-          ++v_uses[s];
+        int prev = -1;
+        int cur = walk.next(v0, v1);
+        for (int u = 0; cur >= 0 || prev >= 0; ++u) {
+          const int s = u % NS;
+          if (!mbar_wait(&kv_empty[s], ((u / NS) & 1) ^ 1, &abort_flag, p.status, 11)) break;
+          mbar_arrive_expect_tx(&kv_full[s], (prev >= 0 ? C::kTile : 0) + (cur >= 0 ? C::kTile : 0));
+          if (prev >= 0)
+            for (int a = 0; a < ATOMS; ++a)
+              tma_load_4d(sV + ((u - 1) % NS) * C::kTile + a * ATOM_BYTES, &tv, &kv_full[s], a * 64, prev, hkv, b);
+          if (cur >= 0)
+            for (int a = 0; a < ATOMS; ++a)
+              tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &kv_full[s], a * 64, cur, hkv, b);
+          ++uses[s];
+          prev = cur;
+          cur = cur >= 0 ? walk.next(v0, v1) : -1;
         }
         if (abort_flag) {
           // let the copies already issued land before the CTA exits
           mbar_wait_drain(&q_full, 0, 200000000ll);
-          for (int s = 0; s < NS; ++s) {
-            if (k_uses[s]) mbar_wait_drain(&k_full[s], (k_uses[s] - 1) & 1, 200000000ll);
-            if (v_uses[s]) mbar_wait_drain(&v_full[s], (v_uses[s] - 1) & 1, 200000000ll);
-          }
+          for (int s = 0; s < NS; ++s)
+            if (uses[s]) mbar_wait_drain(&kv_full[s], (uses[s] - 1) & 1, 200000000ll);
         }
       }
       __syncwarp();
@@ -281,63 +293,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(d_o, a_p + kk * 8, b0 + (uint64_t)(kk * 2048 >> 4), ID_PV, (acc || kk > 0) ? 1u : 0u);
-          mma_commit(&o_done[w]);
         };
+        // Chunk i: its S products are issued one step ahead of its PV
+        // products.  Step i waits for load unit i + 1 (V(i), K(i + 1)) and
+        // issues O0 += P0(i) V(i), S0(i+1), O1 += P1(i) V(i), S1(i+1).  The
+        // commit of s_full[w] after S_w also covers every earlier PV of group
+        // w, so a softmax group that sees its next S may rescale its O rows.
         bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
         int pv_count[2] = {0, 0};
-        // chunk i: (n0, v0, v1); the S products of chunk i are issued before
-        // the PV products of chunk i - 1
         bool cv0 = false, cv1 = false;
         int cur = ok ? walk.next(cv0, cv1) : -1;
-        int i = 0;
         if (cur >= 0) {
-          ok = mbar_wait(&k_full[0], 0, &abort_flag, p.status, 22);
+          ok = mbar_wait(&kv_full[0], 0, &abort_flag, p.status, 22);
           if (ok) {
             tc_fence_after();
             if (cv0) issue_s(0, 0);
             if (cv1) issue_s(1, 0);
-            mma_commit(&k_empty[0]);
+            mma_commit(&kv_empty[0]);
           }
         }
-        while (ok && cur >= 0) {
-          const int s = i % NS;
+        for (int i = 0; ok && cur >= 0; ++i) {
+          const int un = i + 1, su = un % NS;
+          const int s = i % NS, sn = un % NS;
           bool nv0 = false, nv1 = false;
           const int nxt = walk.next(nv0, nv1);
-          const int sn = (i + 1) % NS;
-          if (!mbar_wait(&v_full[s], (i / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
+          if (!mbar_wait(&kv_full[su], (un / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
+          tc_fence_after();
           if (cv0) {
             if (!mbar_wait(&p_full[0], pv_count[0] & 1, &abort_flag, p.status, 25)) { ok = false; break; }
             tc_fence_after();
             issue_pv(0, s, pv_count[0] > 0);
             ++pv_count[0];
           }
-          if (nxt >= 0 && !mbar_wait(&k_full[sn], ((i + 1) / NS) & 1, &abort_flag, p.status, 24)) {
-            ok = false;
-            break;
-          }
-          if (nxt >= 0 && nv0) {
-            tc_fence_after();
-            issue_s(0, sn);
-          }
+          if (nxt >= 0 && nv0) issue_s(0, sn);
           if (cv1) {
             if (!mbar_wait(&p_full[1], pv_count[1] & 1, &abort_flag, p.status, 26)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, s, pv_count[1] > 0);
             ++pv_count[1];
           }
-          if (nxt >= 0) {
-            if (nv1) {
-              tc_fence_after();
-              issue_s(1, sn);
-            }
-            mma_commit(&k_empty[sn]);
-          }
-          mma_commit(&v_empty[s]);
+          if (nxt >= 0 && nv1) issue_s(1, sn);
+          mma_commit(&kv_empty[su]);
           cur = nxt;
           cv0 = nv0;
           cv1 = nv1;
-          ++i;
         }
+        // the epilogues read O once every product is done
+        mma_commit(&o_done[0]);
+        mma_commit(&o_done[1]);
         // all issued MMAs complete before TMEM is released
         mma_commit(&drain);
         mbar_wait_drain(&drain, 0, 200000000ll);
@@ -425,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l = l * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       if (__any_sync(0xffffffffu, rescale)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (i - 1) & 1, &abort_flag, p.status, 32));
-        if (!ok) break;
-        tc_fence_after();
+        // the s_full phase just waited for also covers this group's earlier
+        // PV products, and the next one is issued only after p_full below
+
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O / l -> global, lse
     if (__all_sync(0xffffffffu, ok && !abort_flag)) {
       bool have = true;
-      if (i > 0) have = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (i - 1) & 1, &abort_flag, p.status, 33));
+      if (i > 0) have = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], 0, &abort_flag, p.status, 33));
       tc_fence_after();
       if (have) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
