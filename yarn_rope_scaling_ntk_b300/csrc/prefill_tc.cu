@@ -13,7 +13,8 @@
 // head); both tiles share every key/value tile the CTA loads.  Roles:
 //   warp 9     TMA producer: Q0 and Q1 once, then K and V tiles of 128 keys
 //              into two-stage rings of 128-byte-swizzled shared memory.
-//   warp 8     TMEM owner and MMA issuer (one thread).  For key tile j it
+//   warp 8     TMEM owner and MMA issuer: the warp runs the loop converged
+//              and one elected lane issues the MMAs.  For key tile j it
 //              issues, in this order, O0 += P0(j) V(j), S0(j+1) = Q0 K(j+1)^T,
 //              O1 += P1(j) V(j), S1(j+1) = Q1 K(j+1)^T, so that while one
 //              softmax group works on its S the tensor pipe runs the other
@@ -269,7 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ---------------- MMA issuer ----------------
-      if (lane == 0) {
+      // The whole warp runs the loop (waits, walk, descriptors: warp-uniform
+      // values) and one elected lane issues each group of MMAs and commits.
+      {
+        const bool leader = elect_one();
         // Shared-memory descriptors of every operand buffer, built once; a
         // K step adds its (compile-time) byte offset / 16 to the start
         // address field, which cannot carry out (shared addresses < 256 KB).
@@ -280,72 +284,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](int w, int s) {
           const uint64_t a0 = dq + (w ? kTile16 : 0), b0 = dk + (uint64_t)s * kTile16;
           const uint32_t d_s = tmem + w * S_COLS;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
-            mma_ss(d_s, a0 + off, b0 + off, ID_QK, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+              mma_ss(d_s, a0 + off, b0 + off, ID_QK, kk > 0);
+            }
+            mma_commit(&s_full[w]);
           }
-          mma_commit(&s_full[w]);
+          __syncwarp();
         };
         auto issue_pv = [&](int w, int s, bool acc) {
           const uint64_t b0 = dv + (uint64_t)s * kTile16;
           const uint32_t d_o = tmem + O_COL + w * D, a_p = tmem + w * S_COLS;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(d_o, a_p + kk * 8, b0 + (uint64_t)(kk * 2048 >> 4), ID_PV, (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(d_o, a_p + kk * 8, b0 + (uint64_t)(kk * 2048 >> 4), ID_PV, (acc || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
         };
-        // Chunk i: its S products are issued one step ahead of its PV
-        // products.  Step i waits for load unit i + 1 (V(i), K(i + 1)) and
-        // issues O0 += P0(i) V(i), S0(i+1), O1 += P1(i) V(i), S1(i+1).  The
-        // commit of s_full[w] after S_w also covers every earlier PV of group
-        // w, so a softmax group that sees its next S may rescale its O rows.
-        bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 21);
+        auto commit = [&](uint64_t* bar) {
+          if (leader) mma_commit(bar);
+          __syncwarp();
+        };
+        auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
+          return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
+        };
+        bool ok = wait(&q_full, 0, 21);
         int pv_count[2] = {0, 0};
-        bool cv0 = false, cv1 = false;
+        bool cv0 = false, cv1 = false, nv0 = false, nv1 = false;
         int cur = ok ? walk.next(cv0, cv1) : -1;
+        int nxt = -1;
         if (cur >= 0) {
-          ok = mbar_wait(&kv_full[0], 0, &abort_flag, p.status, 22);
+          ok = wait(&kv_full[0], 0, 22);
           if (ok) {
             tc_fence_after();
             if (cv0) issue_s(0, 0);
             if (cv1) issue_s(1, 0);
-            mma_commit(&kv_empty[0]);
+            commit(&kv_empty[0]);
+            nxt = walk.next(nv0, nv1);
+            ok = wait(&kv_full[1 % NS], (1 / NS) & 1, 23);
           }
         }
+        // Step i (load unit i + 1 = V(i), K(i + 1) has landed; nxt, nv0, nv1
+        // describe chunk i + 1).  The walk and the wait for the next unit come
+        // after S1(i + 1) is queued, while the tensor pipe still has work.
         for (int i = 0; ok && cur >= 0; ++i) {
-          const int un = i + 1, su = un % NS;
-          const int s = i % NS, sn = un % NS;
-          bool nv0 = false, nv1 = false;
-          const int nxt = walk.next(nv0, nv1);
-          if (!mbar_wait(&kv_full[su], (un / NS) & 1, &abort_flag, p.status, 23)) { ok = false; break; }
+          const int s = i % NS, sn = (i + 1) % NS;
           tc_fence_after();
           if (cv0) {
-            if (!mbar_wait(&p_full[0], pv_count[0] & 1, &abort_flag, p.status, 25)) { ok = false; break; }
+            if (!wait(&p_full[0], pv_count[0] & 1, 25)) { ok = false; break; }
             tc_fence_after();
             issue_pv(0, s, pv_count[0] > 0);
             ++pv_count[0];
           }
           if (nxt >= 0 && nv0) issue_s(0, sn);
           if (cv1) {
-            if (!mbar_wait(&p_full[1], pv_count[1] & 1, &abort_flag, p.status, 26)) { ok = false; break; }
+            if (!wait(&p_full[1], pv_count[1] & 1, 26)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, s, pv_count[1] > 0);
             ++pv_count[1];
           }
           if (nxt >= 0 && nv1) issue_s(1, sn);
-          mma_commit(&kv_empty[su]);
+          commit(&kv_empty[sn]);
           cur = nxt;
           cv0 = nv0;
           cv1 = nv1;
+          if (cur >= 0) {
+            nv0 = nv1 = false;
+            nxt = walk.next(nv0, nv1);
+            const int un = i + 2;
+            if (!wait(&kv_full[un % NS], (un / NS) & 1, 24)) { ok = false; break; }
+          }
         }
         // the epilogues read O once every product is done
-        mma_commit(&o_done[0]);
-        mma_commit(&o_done[1]);
+        commit(&o_done[0]);
+        commit(&o_done[1]);
         // all issued MMAs complete before TMEM is released
-        mma_commit(&drain);
-        mbar_wait_drain(&drain, 0, 200000000ll);
+        commit(&drain);
+        if (leader) mbar_wait_drain(&drain, 0, 200000000ll);
+        __syncwarp();
       }
-      __syncwarp();
     }
   } else {
     reg_alloc<kRegsSoftmax>();
