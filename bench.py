@@ -36,6 +36,36 @@ from yarn_rope_scaling_ntk_b300 import api, workloads as W  # noqa: E402
 
 METRIC = "fused YaRN-RoPE+attention TFLOP/s & % bf16 peak; decode HBM GB/s"
 
+CSRC = os.path.join(ROOT, "yarn_rope_scaling_ntk_b300", "csrc")
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of each kernel on the bench's workload, keyed by a hash of
+# the kernel's source files at capture time.  A kernel whose sources changed
+# since reports null.  The commands are in profiles/.
+KERNEL_SOURCES = {
+    "prefill_tc": ("prefill_tc.cu", "tc_ptx.cuh"),
+    "decode": ("decode.cu", "tc_ptx.cuh", "common.cuh"),
+    "rope": ("rope.cu", "common.cuh"),
+}
+TRAFFIC = {
+    # kernel: (source hash, bytes per launch, what was captured)
+}
+
+
+def source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic(kernel: str):
+    rec = TRAFFIC.get(kernel)
+    if rec is None or rec[0] != source_hash(kernel):
+        return None
+    return rec[1]
+
 
 def peaks():
     try:
@@ -60,6 +90,22 @@ def visible_pairs(S: int, mask: str, sink: int, window: int) -> int:
 
 def prefill_flops(w) -> float:
     return 4.0 * w.d * visible_pairs(w.S, w.mask, w.sink, w.window) * w.B * w.Hq
+
+
+def reduce_max(value: float, dist=None, device="cpu") -> float:
+    """Max of a per-rank value over all ranks (the slowest rank's time); the
+    value itself when there is no process group."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Weak scaling: every rank runs the same per-rank work; the job's rate is
+    all ranks' work divided by the slowest rank's time (units per second)."""
+    return work_per_step * steps * world / (max_total_ms * 1e-3)
 
 
 def cfg_of(w):
@@ -205,6 +251,27 @@ def cpu_oracle_prefill(w, seconds: float = 12.0, seed: int = 0):
     return flops / dt / 1e12, desc, threads
 
 
+def time_prefill_workload(w, dev, stream, reps: int = 3):
+    """Device time of the whole fused call (rotation pass + attention) on one
+    of the other prefill workloads; returns a JSON-ready dict."""
+    cfg = cfg_of(w)
+    q, k, v = W.prefill_inputs(w, dev)
+    o = torch.empty_like(q)
+    ws = torch.empty(api.prefill_workspace_bytes(cfg, q.dtype, w.B, w.Hq, w.Hkv, w.S, w.d),
+                     dtype=torch.uint8, device=dev)
+    call = lambda: api.attn_fwd_prefill(cfg, q, k, v, mask=w.mask, sink=w.sink, window=w.window,
+                                        ring_blocks=w.ring_blocks, out=o, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    ms = statistics.median(timed(call, reps, stream))
+    api.sync_status()
+    flops = prefill_flops(w)
+    del q, k, v, o, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "TFLOP": flops / 1e12,
+            "ring_blocks": w.ring_blocks, "mask": w.mask}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -263,13 +330,9 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         times = timed(step, args.steps, stream)
     api.sync_status()
-    total_ms = sum(times)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(times), dist, dev)
     flops = prefill_flops(w)
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
     ms_per_step = total_ms / args.steps
 
     # attention kernel alone (pre-rotated operands, same kernel): roofline
@@ -328,6 +391,16 @@ def run_ours(args):
     rope_bytes = 2 * 2 * q.numel() * 2
     rope_gbs = rope_bytes / (rope_ms * 1e-3) / 1e9
     api.sync_status()
+    del o
+    torch.cuda.empty_cache()
+
+    # ---- the other prefill workloads (whole fused call, device time) -------
+    others = []
+    if not args.no_other_workloads:
+        for wo in (W.RING_128K, W.LLAMA3_8B_GQA, W.LLAMA3_8B_GQA_SW):
+            r = time_prefill_workload(wo, dev, stream)
+            r["frac_of_burst"] = r["TFLOP/s"] / tf_burst
+            others.append(r)
 
     if rank != 0:
         if dist:
@@ -344,20 +417,23 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "pct_bf16_peak": {"burst": value / world / tf_burst, "sustained": value / world / tf_sust,
                           "peaks": peak_src},
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_sust, "unit": "TFLOP/s",
-                     "frac": attn_tflops / tf_sust, "traffic": None,
-                     "kernel": "attention kernel alone on pre-rotated Q/K (same launch the step makes)",
-                     "kernel_ms": attn_ms, "peak_kind": f"bf16 sustained ({peak_src})"},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_burst, "unit": "TFLOP/s",
+                     "frac": attn_tflops / tf_burst, "traffic": traffic("prefill_tc"),
+                     "kernel": "prefill_tc_kernel alone on pre-rotated Q/K (the launch the step makes)",
+                     "kernel_ms": attn_ms, "peak_kind": f"bf16 burst ({peak_src}; kernel timed alone)",
+                     "frac_of_sustained": attn_tflops / tf_sust},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": cs,
         "decode": {"workload": wd.name, "value": dec_gbs, "unit": "GB/s", "ms": dec_ms,
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
-                                "frac": dec_gbs / hbm, "traffic": None}},
+                                "frac": dec_gbs / hbm, "traffic": traffic("decode")}},
+        "other_prefill_workloads": others,
         "rope_apply": {"workload": "Q and K of " + w.name, "value": rope_gbs, "unit": "GB/s",
                        "ms": rope_ms,
                        "roofline": {"bound": "hbm", "achieved": rope_gbs, "peak": hbm, "unit": "GB/s",
-                                    "frac": rope_gbs / hbm, "traffic": None}},
+                                    "frac": rope_gbs / hbm, "traffic": traffic("rope"),
+                                    "traffic_note": "per launch (one tensor of the pair)"}},
     }
     if not args.no_cpu_baseline:
         v_cpu, desc, threads = cpu_oracle_prefill(w, seconds=12.0)
@@ -405,6 +481,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the ring 128K and GQA prefill workloads")
     ap.add_argument("--part", choices=["prefill", "decode", "rope"], default=None,
                     help="profile one kernel family alone (prints no bench line)")
     ap.add_argument("--small", action="store_true", help="with --part: smaller workload")
