@@ -59,6 +59,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct TcParams {
   int B, Hq, Hkv, S, group, n_pairs;
+  int kv_per_sched;  // KV heads per scheduling group (see the CTA order below)
   int mask, sink, window, ring_blocks, cs;
   float scale_log2;
   void* o;
@@ -193,13 +194,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest CTAs first across all heads: the last query-tile pairs of every
-  // (batch, head) come first in launch order
-  const int BH = p.B * p.Hq;
-  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / BH);
-  const int bh = blockIdx.x % BH;
-  const int b = bh / p.Hq, hq = bh % p.Hq;
-  const int hkv = hq / p.group;
+  // Launch order: the (batch, KV head) pairs are taken in scheduling groups
+  // of kv_per_sched; inside a group, every query head that reads one of its
+  // KV heads runs its heaviest query-tile pairs first (longest-first keeps
+  // the tail short).  CTAs that run together then stream the same K/V tiles,
+  // which stay in L2.
+  const int n_kv = p.B * p.Hkv;
+  const int per_kv = p.n_pairs * p.group;  // CTAs per (batch, KV head)
+  const int g0 = (int)(blockIdx.x / ((unsigned)per_kv * p.kv_per_sched)) * p.kv_per_sched;
+  const int gsz = min(p.kv_per_sched, n_kv - g0);
+  const int r = (int)(blockIdx.x - (unsigned)g0 * per_kv);
+  const int heads = gsz * p.group;  // query heads in this group
+  const int pair = p.n_pairs - 1 - r / heads;
+  const int hg = r % heads;
+  const int bkv = g0 + hg / p.group;  // batch * Hkv + KV head
+  const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
+  const int hq = hkv * p.group + hg % p.group;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -521,6 +531,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -563,6 +583,13 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   memset(&p, 0, sizeof(p));
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.S = a.S; p.group = a.Hq / a.Hkv;
   p.n_pairs = (a.S + 2 * BM - 1) / (2 * BM);
+  {
+    // enough KV heads per scheduling group for about three waves of CTAs
+    const int per_kv = p.n_pairs * p.group;
+    const int n_kv = a.B * a.Hkv;
+    int k = (3 * sm_count() + per_kv - 1) / per_kv;
+    p.kv_per_sched = k < 1 ? 1 : (k > n_kv ? n_kv : k);
+  }
   p.mask = a.mask; p.sink = a.sink; p.window = a.window; p.ring_blocks = a.ring_blocks;
   p.cs = (a.ring_blocks > 1 && (a.S / a.ring_blocks) % BN != 0) ? 64 : BN;
   p.scale_log2 = a.scale_log2;
