@@ -63,13 +63,18 @@ typedef enum {
  *        lambda_i = 2 pi b^(2i/d), plus the attention temperature
  *        mscale = 0.1 ln s + 1 for s > 1 ("Context Window Scaling ...",
  *        Section 3; "Long-context extension: stretching attention past its
- *        training window", NTK-by-parts). */
+ *        training window", NTK-by-parts).
+ * PERDIM: a caller-given factor per dimension, theta'_i = theta_i / lambda_i
+ *        (the non-uniform scale vector of LongRoPE, "Context Window Scaling
+ *        ...", Section 4 and FAQ 4; the search that finds the vector is not
+ *        part of this library).  mscale is 1 unless overridden. */
 typedef enum {
   YR_ROPE_NONE = 0,
   YR_ROPE_PLAIN = 1,
   YR_ROPE_PI = 2,
   YR_ROPE_NTK = 3,
-  YR_ROPE_YARN = 4
+  YR_ROPE_YARN = 4,
+  YR_ROPE_PERDIM = 5
 } yr_rope_kind;
 
 typedef enum { YR_F32 = 0, YR_BF16 = 1 } yr_dtype;
@@ -90,7 +95,10 @@ typedef enum { YR_MASK_CAUSAL = 0, YR_MASK_SINK_WINDOW = 1, YR_MASK_NONE = 2 } y
  * L_target        desired context length; used when s <= 0.
  * s               scale factor; <= 0 means L_target / L_train.
  * ramp_alpha/beta YaRN ramp bounds on r (defaults 1 and 32 when both are 0).
- * mscale_override > 0 replaces the temperature factor. */
+ * mscale_override > 0 replaces the temperature factor.
+ * dim_scale       PERDIM only: host array of d/2 finite factors > 0, read
+ *                 during the call (the caller keeps ownership); ignored by
+ *                 the other kinds. */
 typedef struct {
   int32_t kind;
   int32_t head_dim;
@@ -101,6 +109,7 @@ typedef struct {
   double ramp_alpha;
   double ramp_beta;
   double mscale_override;
+  const double* dim_scale;
 } yr_rope_cfg;
 
 /* Rescaled frequencies, host only, float64 (no device work).

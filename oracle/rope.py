@@ -16,7 +16,7 @@ import math
 
 import numpy as np
 
-KINDS = ("none", "plain", "pi", "ntk", "yarn")
+KINDS = ("none", "plain", "pi", "ntk", "yarn", "perdim")
 
 # Regime classes of a frequency dimension, per "Context Window Scaling ...",
 # Section 3 (Decoupled Frequency Partitioning).
@@ -100,7 +100,7 @@ def mscale(kind: str, s: float) -> float:
 
 
 def inv_freq(kind: str, d: int, b: float, L_train: float = 0.0, L_target: float = 0.0,
-             s: float = 0.0, alpha: float = 1.0, beta: float = 32.0):
+             s: float = 0.0, alpha: float = 1.0, beta: float = 32.0, dim_scale=None):
     """Rescaled rotation frequencies theta'_i, regime classes and mscale.
 
     * ``none``  -- theta' = 0: the rotation is the identity (inputs arrive
@@ -117,6 +117,12 @@ def inv_freq(kind: str, d: int, b: float, L_train: float = 0.0, L_target: float 
       NTK-by-parts paragraph; "Context Length Extension", YaRN bullets).
       The blend acts on the frequencies, the reading of "blend the two
       treatments".
+    * ``perdim`` -- a caller-given rescale factor per dimension,
+      theta'_i = theta_i / lambda_i: the non-uniform scale vector that
+      LongRoPE's search produces ("Context Window Scaling ...", Section 4,
+      a unique scale vector for each dimension; FAQ 4, factors of the
+      high-frequency dimensions kept near 1).  The search itself is not part
+      of this path.  The page gives no temperature for it: mscale = 1.
 
     Returns ``(theta_prime[d/2] float64, classes[d/2] int8, mscale float)``.
     """
@@ -129,6 +135,11 @@ def inv_freq(kind: str, d: int, b: float, L_train: float = 0.0, L_target: float 
         return np.zeros(h), cls, 1.0
     if kind == "plain":
         return theta, cls, 1.0
+    if kind == "perdim":
+        lam = np.asarray(dim_scale, dtype=np.float64)
+        if lam.shape != (h,) or not np.all(np.isfinite(lam)) or not np.all(lam > 0):
+            raise ValueError("perdim needs d/2 finite factors > 0")
+        return theta / lam, cls, 1.0
     s = resolve_scale(L_train, L_target, s)
     if kind == "pi":
         return theta / s, cls, 1.0
@@ -166,10 +177,10 @@ def rotate(x: np.ndarray, positions: np.ndarray, theta: np.ndarray) -> np.ndarra
 
 
 def rope_apply(x, positions, kind, d, b, L_train=0.0, L_target=0.0, s=0.0,
-               alpha=1.0, beta=32.0, apply_mscale=False):
+               alpha=1.0, beta=32.0, apply_mscale=False, dim_scale=None):
     """Rotate ``x`` [..., S, d] with the rescaled frequencies; optionally
     multiply by mscale (the temperature split evenly over q and k: q.k then
     carries mscale^2 = 1/t)."""
-    theta, _, ms = inv_freq(kind, d, b, L_train, L_target, s, alpha, beta)
+    theta, _, ms = inv_freq(kind, d, b, L_train, L_target, s, alpha, beta, dim_scale)
     y = rotate(x, positions, theta)
     return y * ms if apply_mscale else y

@@ -147,3 +147,17 @@ def test_library_is_the_product_path():
         if f.endswith(".py"):
             assert "import oracle" not in open(os.path.join(ROOT, "yarn_rope_scaling_ntk_b300", f)).read()
     assert importlib.util.find_spec("yarn_rope_scaling_ntk_b300.api") is not None
+
+
+def test_perdim_inv_freq_matches_oracle_and_rejects_bad_vectors(lib):
+    lam = np.concatenate([np.ones(16), np.linspace(1.0, 6.0, 32), np.full(16, 6.0)])
+    cfg = api.RopeConfig(kind="perdim", head_dim=128, L_train=4096, dim_scale=tuple(lam))
+    th, cls, ms = api.yarn_inv_freq(cfg)
+    th_o, cls_o, ms_o = R.inv_freq("perdim", 128, 1e4, 4096, dim_scale=lam)
+    np.testing.assert_array_equal(cls, cls_o)
+    np.testing.assert_allclose(th, th_o, rtol=1e-15, atol=0)
+    assert ms == ms_o == 1.0
+    for bad in (None, tuple([1.0] * 63 + [0.0]), tuple([1.0] * 63 + [float("inf")]), tuple([-1.0] * 64)):
+        with pytest.raises(api.YarnAttnError) as e:
+            api.yarn_inv_freq(api.RopeConfig(kind="perdim", head_dim=128, L_train=4096, dim_scale=bad))
+        assert e.value.status == 1

@@ -204,3 +204,37 @@ def test_resolve_scale():
     assert rope.resolve_scale(4096, 16384, 2.0) == 2.0
     with pytest.raises(ValueError):
         rope.resolve_scale(0, 0, 0)
+
+
+# ---- per-dimension scale vector (the form LongRoPE's search produces) -------
+
+@pytest.mark.parametrize("d,b,L,s", CONFIG_SHAPES)
+def test_perdim_uniform_vector_is_pi_and_ones_is_plain(d, b, L, s):
+    h = d // 2
+    th_pi, _, _ = rope.inv_freq("pi", d, b, L, 0, s)
+    th_v, cls, ms = rope.inv_freq("perdim", d, b, L, dim_scale=np.full(h, s))
+    np.testing.assert_allclose(th_v, th_pi, rtol=1e-15, atol=0)
+    th_1, _, _ = rope.inv_freq("perdim", d, b, L, dim_scale=np.ones(h))
+    np.testing.assert_array_equal(th_1, rope.base_frequencies(d, b))
+    assert ms == 1.0
+
+
+@pytest.mark.parametrize("d,b,L,s", CONFIG_SHAPES)
+def test_perdim_reproduces_yarn_with_its_equivalent_vector(d, b, L, s):
+    """YaRN is one particular non-uniform vector: the factor of dimension i is
+    theta_i / theta'_i = 1 / ((1 - g_i) / s + g_i), with g_i from the ramp on
+    r_i = L_train / lambda_i (written out here from the definitions)."""
+    h = d // 2
+    i = np.arange(h)
+    r = L / (2 * math.pi * b ** (2.0 * i / d))
+    g = np.clip((r - 1.0) / 31.0, 0.0, 1.0)
+    lam = 1.0 / ((1 - g) / s + g)
+    th_v, _, _ = rope.inv_freq("perdim", d, b, L, dim_scale=lam)
+    th_y, _, _ = rope.inv_freq("yarn", d, b, L, 0, s)
+    np.testing.assert_allclose(th_v, th_y, rtol=1e-14)
+
+
+def test_perdim_rejects_bad_vectors():
+    for bad in (None, np.ones(3), np.array([1.0] * 31 + [0.0]), np.array([1.0] * 31 + [np.nan])):
+        with pytest.raises((ValueError, TypeError)):
+            rope.inv_freq("perdim", 64, 1e4, 64, dim_scale=bad)

@@ -15,10 +15,10 @@ from yarn_rope_scaling_ntk_b300 import api, workloads as W
 pytestmark = gpu
 
 
-def cfg_of(w):
+def cfg_of(w, dim_scale=None):
     r = w.rope
     return api.RopeConfig(kind=r.kind, head_dim=w.d, theta_base=r.theta_base, L_train=r.L_train,
-                          L_target=r.L_target, s=r.s)
+                          L_target=r.L_target, s=r.s, dim_scale=dim_scale)
 
 
 def oracle_prefill(w, q, k, v, rows_per_head, extra_rows=()):
@@ -140,3 +140,26 @@ def test_llama3_8b_gqa_sampled_rows(wl):
     need_cuda()
     q, k, v = W.prefill_inputs(wl, "cuda")
     check(wl, q, k, v, 4, extra_rows=(8191, 8192, 8193, 8194, 8195, 8196, 8197, 16384))
+
+
+def test_perdim_scale_vector_prefill_all_rows():
+    """Attention with a per-dimension scale vector (LongRoPE's form) on the
+    rotation, every row of a small ragged workload."""
+    need_cuda()
+    w = W.Prefill("perdim", 62, 1, 4, 2, 390, 128, torch.bfloat16, W.RopeSpec("perdim", 1e4, 128, 0, 0.0),
+                  "causal")
+    lam = np.concatenate([np.ones(20), np.linspace(1.0, 8.0, 30), np.full(14, 8.0)])
+    q, k, v = W.prefill_inputs(w, "cuda")
+    o, lse = api.attn_fwd_prefill(cfg_of(w, tuple(lam)), q, k, v, return_lse=True)
+    torch.cuda.synchronize()
+    th, _, _ = R.inv_freq("perdim", w.d, 1e4, 128, dim_scale=lam)
+    scale = 1.0 / math.sqrt(w.d)
+    got, want, gl, wl = [], [], [], []
+    for h in range(w.Hq):
+        rows = np.arange(w.S)
+        kr = R.rotate(f64(k[0, h // 2]), rows, th)
+        qr = R.rotate(f64(q[0, h]), rows, th)
+        oo, ll = A.attention_rows(qr, rows, kr, f64(v[0, h // 2]), "causal", 0, 0, scale)
+        got.append(f64(o[0, h])); want.append(oo); gl.append(f64(lse[0, h])); wl.append(ll)
+    assert_attn_close(np.concatenate(got), np.concatenate(want), "perdim")
+    assert_lse_close(np.concatenate(gl), np.concatenate(wl), "perdim")

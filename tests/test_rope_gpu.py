@@ -99,3 +99,18 @@ def test_rope_small_and_empty():
         y = api.rope_apply(_cfg("plain", d, 1e4, 0), x, pos0=7)
         want = R.rotate(f64(x), np.arange(33) + 7, R.base_frequencies(d, 1e4))
         assert np.abs(f64(y) - want).max() <= ROPE_F32_ATOL
+
+
+def test_rope_perdim_scale_vector_f32():
+    """A per-dimension scale vector (LongRoPE's form) through the rotation."""
+    need_cuda()
+    w = W.TINY
+    q, _, _ = W.prefill_inputs(w, "cuda")
+    lam = np.concatenate([np.ones(8), np.linspace(1.0, 4.0, 16), np.full(8, 4.0)])
+    cfg = api.RopeConfig(kind="perdim", head_dim=w.d, theta_base=w.rope.theta_base, L_train=w.rope.L_train,
+                         dim_scale=tuple(lam))
+    y = api.rope_apply(cfg, q, pos0=1000)
+    torch.cuda.synchronize()
+    want = R.rope_apply(f64(q), np.arange(w.S) + 1000, "perdim", w.d, w.rope.theta_base, w.rope.L_train,
+                        dim_scale=lam)
+    assert np.abs(f64(y) - want).max() <= ROPE_F32_ATOL

@@ -19,7 +19,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libyarn_attn.so"
 
-KIND = {"none": 0, "plain": 1, "pi": 2, "ntk": 3, "yarn": 4}
+KIND = {"none": 0, "plain": 1, "pi": 2, "ntk": 3, "yarn": 4, "perdim": 5}
 MASK = {"causal": 0, "sink_window": 1, "none": 2}
 F32, BF16 = 0, 1
 STATUS = {0: "YR_OK", 1: "YR_ERR_INVALID_ARG", 2: "YR_ERR_UNSUPPORTED", 3: "YR_ERR_CUDA",
@@ -37,14 +37,15 @@ class _Cfg(ctypes.Structure):
                 ("theta_base", ctypes.c_double), ("L_train", ctypes.c_int32),
                 ("L_target", ctypes.c_int32), ("s", ctypes.c_double),
                 ("ramp_alpha", ctypes.c_double), ("ramp_beta", ctypes.c_double),
-                ("mscale_override", ctypes.c_double)]
+                ("mscale_override", ctypes.c_double), ("dim_scale", ctypes.POINTER(ctypes.c_double))]
 
 
 @dataclass(frozen=True)
 class RopeConfig:
     """The pages' problem statement: rescaling kind, head dim d, base b,
-    L_train, L_target, scale s (<= 0: L_target / L_train), YaRN ramp bounds
-    and an optional temperature override."""
+    L_train, L_target, scale s (<= 0: L_target / L_train), YaRN ramp bounds,
+    an optional temperature override, and (kind "perdim") the d/2 factors of
+    a per-dimension scale vector."""
     kind: str = "yarn"
     head_dim: int = 128
     theta_base: float = 10000.0
@@ -54,13 +55,19 @@ class RopeConfig:
     ramp_alpha: float = 1.0
     ramp_beta: float = 32.0
     mscale_override: float = 0.0
+    dim_scale: tuple | None = None
 
     def c(self) -> _Cfg:
         if self.kind not in KIND:
             raise ValueError(f"unknown rope kind {self.kind!r}")
-        return _Cfg(KIND[self.kind], int(self.head_dim), float(self.theta_base), int(self.L_train),
-                    int(self.L_target), float(self.s), float(self.ramp_alpha),
-                    float(self.ramp_beta), float(self.mscale_override))
+        cfg = _Cfg(KIND[self.kind], int(self.head_dim), float(self.theta_base), int(self.L_train),
+                   int(self.L_target), float(self.s), float(self.ramp_alpha),
+                   float(self.ramp_beta), float(self.mscale_override), None)
+        if self.dim_scale is not None:
+            arr = (ctypes.c_double * len(self.dim_scale))(*[float(v) for v in self.dim_scale])
+            cfg._dim_scale_buf = arr  # keeps the array alive with the struct
+            cfg.dim_scale = ctypes.cast(arr, ctypes.POINTER(ctypes.c_double))
+        return cfg
 
 
 _lib = None

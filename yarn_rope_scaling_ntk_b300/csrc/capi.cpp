@@ -39,11 +39,13 @@ static const double kTwoPi = 6.283185307179586476925286766559;
 //            g = clamp((r-alpha)/(beta-alpha)), r = L_train / lambda_i,
 //            lambda_i = 2 pi b^(2i/d)
 //  mscale    0.1 ln s + 1 (YaRN, s > 1)  same page, Section 3 and its listing
+//  PERDIM    theta_i / lambda_i          same page, Section 4 (a scale vector
+//                                        per dimension, caller-given)
 yr_status compute_inv_freq(const yr_rope_cfg* cfg, int d, double* theta, int8_t* cls,
                            double* mscale) {
   if (!cfg) return fail(YR_ERR_INVALID_ARG, "cfg is NULL");
   const int kind = cfg->kind;
-  if (kind < YR_ROPE_NONE || kind > YR_ROPE_YARN)
+  if (kind < YR_ROPE_NONE || kind > YR_ROPE_PERDIM)
     return fail(YR_ERR_INVALID_ARG, "unknown rope kind %d", kind);
   if (d < 2 || (d & 1)) return fail(YR_ERR_INVALID_ARG, "head dimension %d must be even and >= 2", d);
   if (d / 2 > kMaxHalf) return fail(YR_ERR_UNSUPPORTED, "head dimension %d above %d", d, 2 * kMaxHalf);
@@ -67,6 +69,12 @@ yr_status compute_inv_freq(const yr_rope_cfg* cfg, int d, double* theta, int8_t*
     }
   }
   if (kind == YR_ROPE_YARN && cfg->L_train <= 0) return fail(YR_ERR_INVALID_ARG, "YaRN needs L_train > 0");
+  if (kind == YR_ROPE_PERDIM) {
+    if (!cfg->dim_scale) return fail(YR_ERR_INVALID_ARG, "PERDIM needs dim_scale (d/2 factors)");
+    for (int i = 0; i < d / 2; ++i)
+      if (!(cfg->dim_scale[i] > 0.0) || !isfinite(cfg->dim_scale[i]))
+        return fail(YR_ERR_INVALID_ARG, "dim_scale[%d] must be finite and > 0", i);
+  }
   if (kind == YR_ROPE_NTK && d <= 2) return fail(YR_ERR_INVALID_ARG, "NTK scaling needs d > 2");
 
   const int h = d / 2;
@@ -82,6 +90,7 @@ yr_status compute_inv_freq(const yr_rope_cfg* cfg, int d, double* theta, int8_t*
       case YR_ROPE_PLAIN: t = base_i; break;
       case YR_ROPE_PI: t = base_i / s; break;
       case YR_ROPE_NTK: t = pow(bb, -2.0 * i / d); break;
+      case YR_ROPE_PERDIM: t = base_i / cfg->dim_scale[i]; break;
       default: {
         const double g = std::min(1.0, std::max(0.0, (r - alpha) / (beta - alpha)));
         t = (1.0 - g) * base_i / s + g * base_i;

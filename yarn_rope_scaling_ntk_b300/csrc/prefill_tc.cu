@@ -50,9 +50,9 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;               // warps 10 and 11 only lend registers
 // Register budgets (launch: 384 threads x 168).  The softmax groups hold a
 // full 128-column row of S in registers; the control warpgroup keeps the
-// MMA issue loop in registers: 2 x 128 x 192 + 128 x 120 = 64512 = 384 x 168.
-constexpr uint32_t kRegsSoftmax = 192;
-constexpr uint32_t kRegsControl = 120;
+// MMA issue loop in registers: 2 x 128 x 216 + 128 x 72 = 64512 = 384 x 168.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
