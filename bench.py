@@ -48,7 +48,7 @@ KERNEL_SOURCES = {
 }
 TRAFFIC = {
     # kernel: (source hash, bytes per launch, what was captured)
-    "prefill_tc": ("3f9b9e77684830e8", 2.08e9 + 121.08e6,
+    "prefill_tc": ("e12dd2ec64287794", 510.50e6 + 117.03e6,
                    "bench.py --part prefill: Llama-2-7B shape S=16384, one launch"),
     "decode": ("ba6d6bf8234c171d", 4.30e9 + 3.59e6,
                "bench.py --part decode: 64 sequences x 32 heads x 4096 slots, one launch"),
