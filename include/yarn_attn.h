@@ -177,6 +177,52 @@ yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k,
                            float softmax_scale, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Bytes of device workspace attn_fwd_prefill_kv_block needs (0 when none). */
+size_t yr_prefill_kv_block_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B,
+                                           int32_t Hq, int32_t Hkv, int32_t Sq, int32_t Skv, int32_t d);
+
+/* One query block against one key/value block: the computation a device of
+ * a ring does for each KV block it holds ("Context Window Scaling ...",
+ * Section 5: GPU i computes attention of its query block Q_i with the
+ * resident block KV_j; "Context Length Extension", Ring Attention: each GPU
+ * computes partial attention with its local keys).  Query row r sits at
+ * position q_pos0 + r and key n at k_pos0 + n; positions drive both the
+ * rotation and the mask (a block entirely in the future gives o = 0 and
+ * lse = -inf for every row, which attn_merge_partial treats as empty).
+ * q   : device [B, Hq, Sq, d] in_dtype;  k, v : device [B, Hkv, Skv, d].
+ * o   : device [B, Hq, Sq, d] of out_dtype (YR_F32 keeps the partial exact
+ *       for merging; YR_BF16 for a single block).
+ * lse : device float32 [B, Hq, Sq] contiguous, or NULL (a partial to be
+ *       merged needs it).
+ * Other arguments as attn_fwd_prefill; ring order is the caller's (one KV
+ * block per call).  Skv = 0 gives o = 0 and lse = -inf. */
+yr_status attn_fwd_prefill_kv_block(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v,
+                                    void* o, float* lse, int32_t in_dtype, int32_t out_dtype, int32_t B,
+                                    int32_t Hq, int32_t Hkv, int32_t Sq, int32_t Skv, int32_t d,
+                                    int32_t q_pos0, int32_t k_pos0, const int64_t q_strides[3],
+                                    const int64_t k_strides[3], const int64_t v_strides[3],
+                                    const int64_t o_strides[3], int32_t mask, int32_t sink, int32_t window,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* Exact merge of one attention partial into an accumulator, both over
+ * disjoint key sets and normalised over their own keys:
+ *   L = ln(e^La + e^Lp),  O = e^(La - L) Oa + e^(Lp - L) Op
+ * ("Context Length Extension", Ring Attention: partial results are combined
+ * using online softmax).  A side whose lse is -inf is empty and is not read
+ * (so a fresh accumulator needs only lse_acc = -inf).
+ * o_acc    : device float32 [B, H, S, d] (strides acc_strides), updated.
+ * lse_acc  : device float32 [B, H, S] contiguous, updated.
+ * o_part, lse_part : the partial, same shapes (o strides part_strides).
+ * o_final  : optional device [B, H, S, d] of final_dtype (F32 or BF16)
+ *            receiving the merged O as well (NULL: none), strides
+ *            final_strides (8-byte aligned for bf16).
+ * d a multiple of 4; 16-byte-aligned pointers and rows.  Memory-bound. */
+yr_status attn_merge_partial(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                             void* o_final, int32_t final_dtype, int32_t B, int32_t H, int32_t S, int32_t d,
+                             const int64_t acc_strides[3], const int64_t part_strides[3],
+                             const int64_t final_strides[3], void* stream);
+
 /* Split count the decode entry point uses when num_splits <= 0. */
 int32_t yr_decode_auto_splits(int32_t B, int32_t Hkv, int32_t sink, int32_t window);
 

@@ -134,6 +134,30 @@ def fold_blockwise(q_row, q_pos, k, v, blocks, mask, sink, window, scale, k_pos=
     return acc / l, mx + math.log(l)
 
 
+def merge_partials(parts):
+    """Combine attention partials over disjoint key sets, each ``(o [R, d],
+    lse [R])`` normalised over its own keys, into the attention over their
+    union: lse = ln sum_j e^(lse_j), o = sum_j e^(lse_j - lse) o_j ("Context
+    Length Extension", Ring Attention: partial results are combined using
+    online softmax).  Rows where every lse is -inf are empty (o = 0)."""
+    lses = np.stack([np.asarray(l, dtype=np.float64) for _, l in parts])      # [J, R]
+    os_ = np.stack([np.asarray(o, dtype=np.float64) for o, _ in parts])       # [J, R, d]
+    mx = lses.max(axis=0)
+    empty = ~np.isfinite(mx)
+    mx = np.where(empty, 0.0, mx)
+    w = np.exp(lses - mx[None, :])                                          # e^-inf = 0
+    tot = w.sum(axis=0)
+    # an empty partial (lse = -inf) has weight 0 and no defined output: it is
+    # not read at all
+    contrib = np.where((w > 0)[:, :, None], w[:, :, None] * os_, 0.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = mx + np.log(tot)
+        o = contrib.sum(axis=0) / tot[:, None]
+    o[empty] = 0.0
+    lse[empty] = -np.inf
+    return o, lse
+
+
 def prefill_head(q, k, v, rows, theta, scale, mask, sink=0, window=0):
     """Reference for one (batch, head): rotate the selected query rows at
     their positions and every key at its position, then exact attention.

@@ -38,7 +38,8 @@ def assert_lse_close(got, want, what=""):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     both_inf = np.isneginf(got) & np.isneginf(want)
-    err = np.abs(np.where(both_inf, 0.0, got - want)).max() if got.size else 0.0
+    with np.errstate(invalid="ignore"):
+        err = np.abs(np.where(both_inf, 0.0, got - want)).max() if got.size else 0.0
     assert err <= LSE_ATOL, f"{what}: lse max-abs {err:.3e}"
 
 

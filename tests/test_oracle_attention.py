@@ -254,3 +254,40 @@ def test_prefill_head_small():
     for a, m in enumerate(rows):
         ob, lb = _brute(qr[m], kr, v, m, "causal", 0, 0, 0.4)
         np.testing.assert_allclose(o[a], ob, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask,sink,window", [("causal", 0, 0), ("sink_window", 2, 4), ("none", 0, 0)])
+def test_merge_partials_equals_full_attention_by_brute_force(mask, sink, window):
+    """Splitting the keys into blocks (any sizes, some blocks empty for some
+    rows), attending per block and merging equals brute-force attention."""
+    rng = np.random.default_rng(21)
+    S, d = 13, 5
+    q, k, v = rng.standard_normal((3, S, d))
+    scale = 0.9
+    rows = np.arange(S)
+    edges = [0, 3, 4, 9, 13]
+    parts = []
+    for a, b in zip(edges[:-1], edges[1:]):
+        kp = np.arange(a, b)
+        parts.append(A.attention_rows(q, rows, k[a:b], v[a:b], mask, sink, window, scale, k_pos=kp))
+    o, lse = A.merge_partials(parts[::-1])  # any order
+    for m in range(S):
+        ob, lb = _brute(q[m], k, v, m, mask, sink, window, scale)
+        np.testing.assert_allclose(o[m], ob, atol=1e-12)
+        assert lse[m] == pytest.approx(lb, abs=1e-12)
+
+
+def test_merge_partials_lse_is_logsumexp_and_empty_rows():
+    lse_a, lse_b = np.array([0.3, -np.inf, -np.inf]), np.array([-1.2, 2.0, -np.inf])
+    o_a, o_b = np.ones((3, 2)), 2 * np.ones((3, 2))
+    o, lse = A.merge_partials([(o_a, lse_a), (o_b, lse_b)])
+    assert lse[0] == pytest.approx(logsumexp([0.3, -1.2]), abs=1e-15)
+    assert lse[1] == 2.0 and np.all(o[1] == 2.0)
+    assert np.isneginf(lse[2]) and np.all(o[2] == 0.0)
+
+
+def test_merge_partials_ignores_the_output_of_an_empty_partial():
+    o_a = np.full((2, 3), np.nan)
+    o, lse = A.merge_partials([(o_a, np.array([-np.inf, -np.inf])), (np.ones((2, 3)), np.array([0.5, -np.inf]))])
+    assert np.all(o[0] == 1.0) and lse[0] == 0.5
+    assert np.all(o[1] == 0.0) and np.isneginf(lse[1])

@@ -97,6 +97,11 @@ def load_library():
         "attn_fwd_prefill": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32, I32,
                                    _i64x3, _i64x3, _i64x3, _i64x3, I32, I32, I32, I32,
                                    ctypes.c_float, _P, SZ, _P]),
+        "yr_prefill_kv_block_workspace_bytes": (SZ, [cfgp, I32, I32, I32, I32, I32, I32, I32]),
+        "attn_fwd_prefill_kv_block": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32, I32, I32, I32,
+                                            I32, I32, _i64x3, _i64x3, _i64x3, _i64x3, I32, I32, I32,
+                                            ctypes.c_float, _P, SZ, _P]),
+        "attn_merge_partial": (I32, [_P, _P, _P, _P, _P, I32, I32, I32, I32, I32, _i64x3, _i64x3, _i64x3, _P]),
         "yr_decode_auto_splits": (I32, [I32, I32, I32, I32]),
         "yr_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
         "attn_fwd_decode_sinkwindow": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
@@ -204,6 +209,55 @@ def attn_fwd_prefill(cfg: RopeConfig, q, k, v, mask: str = "causal", sink: int =
                                 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                 _stream(stream)))
     return (o, lse) if return_lse else o
+
+
+def attn_fwd_prefill_kv_block(cfg: RopeConfig, q, k, v, q_pos0: int, k_pos0: int, mask: str = "causal",
+                              sink: int = 0, window: int = 0, softmax_scale: float = 0.0,
+                              out_dtype: torch.dtype = torch.float32, out=None, lse=None, workspace=None,
+                              stream=None):
+    """One query block q [B, Hq, Sq, d] (rows at q_pos0 + r) against one KV
+    block k/v [B, Hkv, Skv, d] (keys at k_pos0 + n).  Returns (o, lse); o in
+    ``out_dtype`` (float32 keeps the partial exact for attn_merge_partial)."""
+    lib = load_library()
+    B, Hq, Sq, d = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Skv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Skv, d]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k and v must share a dtype")
+    o = torch.empty(B, Hq, Sq, d, dtype=out_dtype, device=q.device) if out is None else out
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    c = cfg.c()
+    code = F32 if q.dtype == torch.float32 else BF16
+    need = int(lib.yr_prefill_kv_block_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, Sq, Skv, d))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.attn_fwd_prefill_kv_block(
+        ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _dtype_code(q), _dtype_code(o),
+        B, Hq, Hkv, Sq, Skv, d, int(q_pos0), int(k_pos0), _strides(q), _strides(k), _strides(v), _strides(o),
+        MASK[mask], int(sink), int(window), float(softmax_scale), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, lse
+
+
+def attn_merge_partial(o_acc, lse_acc, o_part, lse_part, out=None, stream=None):
+    """Merge the partial (o_part, lse_part) into (o_acc, lse_acc) in place
+    (float32 [B, H, S, d] and [B, H, S]); if ``out`` is given (float32 or
+    bfloat16) it receives the merged O too."""
+    lib = load_library()
+    B, H, S, d = o_acc.shape
+    for t in (o_acc, o_part):
+        if t.dtype != torch.float32 or t.shape != (B, H, S, d):
+            raise ValueError("o_acc and o_part must be float32 [B, H, S, d]")
+    for t in (lse_acc, lse_part):
+        if t.dtype != torch.float32 or t.shape != (B, H, S) or not t.is_contiguous():
+            raise ValueError("lse tensors must be contiguous float32 [B, H, S]")
+    _check(lib.attn_merge_partial(_ptr(o_acc), _ptr(lse_acc), _ptr(o_part), _ptr(lse_part), _ptr(out),
+                                  F32 if out is None else _dtype_code(out), B, H, S, d, _strides(o_acc),
+                                  _strides(o_part), _strides(out) if out is not None else _i64x3(0, 0, 0),
+                                  _stream(stream)))
+    return o_acc, lse_acc
 
 
 def decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits=0) -> int:

@@ -190,50 +190,65 @@ static bool prefill_needs_q_copy(int in_dtype, const yr_rope_cfg* cfg) {
   return in_dtype == YR_F32 || cfg->kind != YR_ROPE_NONE;
 }
 
-size_t yr_prefill_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B, int32_t Hq,
-                                  int32_t Hkv, int32_t S, int32_t d) {
-  if (!cfg || B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || d <= 0) return 0;
-  const size_t row = (size_t)S * d * 2;  // one head of bf16
+static size_t prefill_ws_bytes(const yr_rope_cfg* cfg, int in_dtype, int B, int Hq, int Hkv, int Sq, int Skv,
+                               int d) {
+  if (!cfg || B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0) return 0;
   size_t bytes = 0;
-  if (prefill_needs_q_copy(in_dtype, cfg)) bytes += (size_t)B * Hq * row + (size_t)B * Hkv * row;
-  if (in_dtype == YR_F32) bytes += (size_t)B * Hkv * row;
+  if (prefill_needs_q_copy(in_dtype, cfg))
+    bytes += (size_t)B * Hq * Sq * d * 2 + (size_t)B * Hkv * Skv * d * 2;
+  if (in_dtype == YR_F32) bytes += (size_t)B * Hkv * Skv * d * 2;
   return bytes;
 }
 
-yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v,
-                           void* o, float* lse, int32_t in_dtype, int32_t B, int32_t Hq,
-                           int32_t Hkv, int32_t S, int32_t d, const int64_t q_strides[3],
-                           const int64_t k_strides[3], const int64_t v_strides[3],
-                           const int64_t o_strides[3], int32_t mask, int32_t sink,
-                           int32_t window, int32_t ring_blocks, float softmax_scale,
-                           void* workspace, size_t workspace_bytes, void* stream) {
-  clear_error();
-  if (!cfg) return fail(YR_ERR_INVALID_ARG, "cfg is NULL");
-  if (in_dtype != YR_F32 && in_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "dtype %d", in_dtype);
-  if (B < 0 || Hq < 0 || Hkv < 0 || S < 0) return fail(YR_ERR_INVALID_ARG, "negative shape");
+size_t yr_prefill_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B, int32_t Hq,
+                                  int32_t Hkv, int32_t S, int32_t d) {
+  return prefill_ws_bytes(cfg, in_dtype, B, Hq, Hkv, S, S, d);
+}
+
+size_t yr_prefill_kv_block_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B, int32_t Hq,
+                                           int32_t Hkv, int32_t Sq, int32_t Skv, int32_t d) {
+  return prefill_ws_bytes(cfg, in_dtype, B, Hq, Hkv, Sq, Skv, d);
+}
+
+// Shared body of attn_fwd_prefill and attn_fwd_prefill_kv_block: query rows
+// at positions q_pos0 .. q_pos0 + Sq - 1 against keys at k_pos0 .. k_pos0 +
+// Skv - 1 (positions drive both the rotation and the mask).
+static yr_status prefill_impl(const char* who, const yr_rope_cfg* cfg, const void* q, const void* k,
+                              const void* v, void* o, float* lse, int32_t in_dtype, int32_t out_dtype,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t Sq, int32_t Skv, int32_t d,
+                              int32_t q_pos0, int32_t k_pos0, const int64_t q_strides[3],
+                              const int64_t k_strides[3], const int64_t v_strides[3],
+                              const int64_t o_strides[3], int32_t mask, int32_t sink, int32_t window,
+                              int32_t ring_blocks, float softmax_scale, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!cfg) return fail(YR_ERR_INVALID_ARG, "%s: cfg is NULL", who);
+  if (in_dtype != YR_F32 && in_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "%s: dtype %d", who, in_dtype);
+  if (out_dtype != YR_F32 && out_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "%s: out dtype %d", who, out_dtype);
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0) return fail(YR_ERR_INVALID_ARG, "%s: negative shape", who);
   if (d != 64 && d != 128) return fail(YR_ERR_UNSUPPORTED, "attention head dimension %d (64 or 128)", d);
   if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return fail(YR_ERR_INVALID_ARG, "Hq %% Hkv != 0");
   if (mask < YR_MASK_CAUSAL || mask > YR_MASK_NONE) return fail(YR_ERR_INVALID_ARG, "mask %d", mask);
   if (mask == YR_MASK_SINK_WINDOW && (sink < 0 || window < 1))
     return fail(YR_ERR_INVALID_ARG, "sink must be >= 0 and window >= 1");
   if (ring_blocks < 1) return fail(YR_ERR_INVALID_ARG, "ring_blocks must be >= 1");
-  if (S > (1 << 24)) return fail(YR_ERR_INVALID_ARG, "S above 2^24");
+  if (q_pos0 < 0 || k_pos0 < 0 || (int64_t)q_pos0 + Sq > (1 << 24) || (int64_t)k_pos0 + Skv > (1 << 24))
+    return fail(YR_ERR_INVALID_ARG, "%s: positions must lie in [0, 2^24)", who);
   if (!q_strides || !k_strides || !v_strides || !o_strides) return fail(YR_ERR_INVALID_ARG, "strides are NULL");
   RopeFreqs f;
   yr_status st = build_rope_freqs(cfg, d, &f);
   if (st != YR_OK) return st;
-  if (ring_blocks > 1 && S % ring_blocks != 0)
-    return fail(YR_ERR_INVALID_ARG, "S=%d is not divisible by ring_blocks=%d", S, ring_blocks);
-  if (ring_blocks > 1 && (S / ring_blocks) % 64 != 0)
+  if (ring_blocks > 1 && Skv % ring_blocks != 0)
+    return fail(YR_ERR_INVALID_ARG, "S=%d is not divisible by ring_blocks=%d", Skv, ring_blocks);
+  if (ring_blocks > 1 && (Skv / ring_blocks) % 64 != 0)
     return fail(YR_ERR_UNSUPPORTED, "ring blocks must hold a multiple of 64 keys");
-  if (B == 0 || S == 0) return YR_OK;
-  if (!q || !k || !v || !o) return fail(YR_ERR_INVALID_ARG, "q, k, v or o is NULL");
+  if (B == 0 || Sq == 0) return YR_OK;
+  if (!q || !o || (Skv > 0 && (!k || !v))) return fail(YR_ERR_INVALID_ARG, "q, k, v or o is NULL");
   const int elem = in_dtype == YR_BF16 ? 2 : 4;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      !rows_aligned(q_strides, elem) || !rows_aligned(k_strides, elem) ||
-      !rows_aligned(v_strides, elem) || !rows_aligned(o_strides, elem))
+  const int oelem = out_dtype == YR_BF16 ? 2 : 4;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !rows_aligned(q_strides, elem) ||
+      !rows_aligned(k_strides, elem) || !rows_aligned(v_strides, elem) || !rows_aligned(o_strides, oelem))
     return fail(YR_ERR_INVALID_ARG, "pointers and strides must be 16-byte aligned");
-  const size_t need = yr_prefill_workspace_bytes(cfg, in_dtype, B, Hq, Hkv, S, d);
+  const size_t need = prefill_ws_bytes(cfg, in_dtype, B, Hq, Hkv, Sq, Skv, d);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(YR_ERR_INVALID_ARG, "workspace of %zu bytes needed", need);
   if (need > 0 && !aligned16(workspace)) return fail(YR_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -244,27 +259,35 @@ yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k,
 
   PrefillLaunch p;
   memset(&p, 0, sizeof(p));
-  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.out_bf16 = in_dtype == YR_BF16;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.d = d;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.out_bf16 = out_dtype == YR_BF16;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d;
+  p.Sq = Sq; p.Skv = Skv; p.q_pos0 = q_pos0; p.k_pos0 = k_pos0;
   for (int i = 0; i < 3; ++i) {
     p.qs[i] = q_strides[i]; p.ks[i] = k_strides[i]; p.vs[i] = v_strides[i]; p.os[i] = o_strides[i];
   }
   p.mask = mask; p.sink = sink; p.window = window; p.ring_blocks = ring_blocks;
   p.scale_log2 = (float)(scale * 1.4426950408889634073599246810019);
 
-  // Rotated bfloat16 copies in the workspace, each [B, H, S, d] contiguous:
-  // Q (rotated), K (rotated), and V (converted) for float32 inputs.
+  if (Skv == 0) {
+    // no keys: every row is the empty softmax, o = 0 and lse = -inf
+    cudaError_t e = launch_fill_empty(o, p.out_bf16, lse, B, Hq, Sq, d, o_strides, cs);
+    return e == cudaSuccess ? YR_OK : cuda_fail(e, "attention (empty key set) launch");
+  }
+
+  // Rotated bfloat16 copies in the workspace, each [B, H, rows, d]
+  // contiguous: Q (rotated at q_pos0 + row), K (rotated at k_pos0 + key),
+  // and V (converted) for float32 inputs.
   char* ws = static_cast<char*>(workspace);
   size_t off = 0;
-  const int64_t hs = (int64_t)S * d;
-  auto prep = [&](const void* src, const int64_t* src_s, int H, bool rotate, const void** dst,
-                  int64_t* dst_s) -> cudaError_t {
+  auto prep = [&](const void* src, const int64_t* src_s, int H, int rows, int pos0, bool rotate,
+                  const void** dst, int64_t* dst_s) -> cudaError_t {
     void* out = ws + off;
+    const int64_t hs = (int64_t)rows * d;
     off += (size_t)B * H * hs * 2;
     RopeLaunch a;
     memset(&a, 0, sizeof(a));
     a.x = src; a.y = out; a.in_bf16 = in_dtype == YR_BF16; a.out_bf16 = 1;
-    a.B = B; a.H = H; a.S = S; a.d = d;
+    a.B = B; a.H = H; a.S = rows; a.d = d; a.pos0 = pos0;
     dst_s[0] = (int64_t)H * hs; dst_s[1] = hs; dst_s[2] = d;
     for (int i = 0; i < 3; ++i) { a.xs[i] = src_s[i]; a.ys[i] = dst_s[i]; }
     RopeFreqs ff = f;
@@ -273,13 +296,69 @@ yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k,
     return launch_rope(a, ff, cs);
   };
   if (prefill_needs_q_copy(in_dtype, cfg)) {
-    cudaError_t e = prep(q, q_strides, Hq, true, &p.q, p.qs);
-    if (e == cudaSuccess) e = prep(k, k_strides, Hkv, true, &p.k, p.ks);
-    if (e == cudaSuccess && in_dtype == YR_F32) e = prep(v, v_strides, Hkv, false, &p.v, p.vs);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_prefill rotation pass");
+    cudaError_t e = prep(q, q_strides, Hq, Sq, q_pos0, true, &p.q, p.qs);
+    if (e == cudaSuccess) e = prep(k, k_strides, Hkv, Skv, k_pos0, true, &p.k, p.ks);
+    if (e == cudaSuccess && in_dtype == YR_F32) e = prep(v, v_strides, Hkv, Skv, 0, false, &p.v, p.vs);
+    if (e != cudaSuccess) return cuda_fail(e, "attention rotation pass");
   }
   cudaError_t e = launch_prefill(p, cs);
-  return e == cudaSuccess ? YR_OK : cuda_fail(e, "attn_fwd_prefill launch");
+  return e == cudaSuccess ? YR_OK : cuda_fail(e, "attention launch");
+}
+
+yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v,
+                           void* o, float* lse, int32_t in_dtype, int32_t B, int32_t Hq,
+                           int32_t Hkv, int32_t S, int32_t d, const int64_t q_strides[3],
+                           const int64_t k_strides[3], const int64_t v_strides[3],
+                           const int64_t o_strides[3], int32_t mask, int32_t sink,
+                           int32_t window, int32_t ring_blocks, float softmax_scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (S > (1 << 24)) return fail(YR_ERR_INVALID_ARG, "S above 2^24");
+  return prefill_impl("attn_fwd_prefill", cfg, q, k, v, o, lse, in_dtype, in_dtype, B, Hq, Hkv, S, S, d, 0, 0,
+                      q_strides, k_strides, v_strides, o_strides, mask, sink, window, ring_blocks, softmax_scale,
+                      workspace, workspace_bytes, stream);
+}
+
+yr_status attn_fwd_prefill_kv_block(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v,
+                                    void* o, float* lse, int32_t in_dtype, int32_t out_dtype, int32_t B,
+                                    int32_t Hq, int32_t Hkv, int32_t Sq, int32_t Skv, int32_t d,
+                                    int32_t q_pos0, int32_t k_pos0, const int64_t q_strides[3],
+                                    const int64_t k_strides[3], const int64_t v_strides[3],
+                                    const int64_t o_strides[3], int32_t mask, int32_t sink, int32_t window,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  clear_error();
+  return prefill_impl("attn_fwd_prefill_kv_block", cfg, q, k, v, o, lse, in_dtype, out_dtype, B, Hq, Hkv, Sq,
+                      Skv, d, q_pos0, k_pos0, q_strides, k_strides, v_strides, o_strides, mask, sink, window, 1,
+                      softmax_scale, workspace, workspace_bytes, stream);
+}
+
+yr_status attn_merge_partial(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part,
+                             void* o_final, int32_t final_dtype, int32_t B, int32_t H, int32_t S, int32_t d,
+                             const int64_t acc_strides[3], const int64_t part_strides[3],
+                             const int64_t final_strides[3], void* stream) {
+  clear_error();
+  if (B < 0 || H < 0 || S < 0) return fail(YR_ERR_INVALID_ARG, "attn_merge_partial: negative shape");
+  if (d <= 0 || d % 4 != 0 || d > 1024) return fail(YR_ERR_UNSUPPORTED, "attn_merge_partial: d=%d (a multiple of 4 up to 1024)", d);
+  if (final_dtype != YR_F32 && final_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "final dtype %d", final_dtype);
+  if ((int64_t)B * H * S == 0) return YR_OK;
+  if (!o_acc || !lse_acc || !o_part || !lse_part || !acc_strides || !part_strides)
+    return fail(YR_ERR_INVALID_ARG, "attn_merge_partial: a required pointer is NULL");
+  if (o_final && !final_strides) return fail(YR_ERR_INVALID_ARG, "attn_merge_partial: final strides are NULL");
+  const int felem = final_dtype == YR_BF16 ? 2 : 4;
+  if (!aligned16(o_acc) || !aligned16(o_part) || !rows_aligned(acc_strides, 4) || !rows_aligned(part_strides, 4) ||
+      (o_final && (((uintptr_t)o_final & 7) != 0 || !rows_aligned(final_strides, felem))))
+    return fail(YR_ERR_INVALID_ARG, "attn_merge_partial: pointers and strides must be 16-byte aligned");
+  MergeLaunch m;
+  memset(&m, 0, sizeof(m));
+  m.o_acc = o_acc; m.lse_acc = lse_acc; m.o_part = o_part; m.lse_part = lse_part;
+  m.o_final = o_final; m.final_bf16 = final_dtype == YR_BF16;
+  m.B = B; m.H = H; m.S = S; m.d = d;
+  for (int i = 0; i < 3; ++i) {
+    m.as[i] = acc_strides[i]; m.ps[i] = part_strides[i]; m.fs[i] = o_final ? final_strides[i] : 0;
+  }
+  cudaError_t e = launch_merge(m, as_stream(stream));
+  return e == cudaSuccess ? YR_OK : cuda_fail(e, "attn_merge_partial launch");
 }
 
 int32_t yr_decode_auto_splits(int32_t B, int32_t Hkv, int32_t sink, int32_t window) {

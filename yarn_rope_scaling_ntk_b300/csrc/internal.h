@@ -71,11 +71,29 @@ struct PrefillLaunch {
   void* o;
   float* lse;
   int out_bf16;
-  int B, Hq, Hkv, S, d;
+  int B, Hq, Hkv, d;
+  int Sq, Skv;         // query rows and keys
+  int q_pos0, k_pos0;  // positions of query row 0 and key 0 (mask)
   int64_t qs[3], ks[3], vs[3], os[3];
   int mask, sink, window, ring_blocks;
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t st);
+
+// Exact merge of an attention partial into an accumulator (attn_merge_partial).
+struct MergeLaunch {
+  float* o_acc;
+  float* lse_acc;
+  const float* o_part;
+  const float* lse_part;
+  void* o_final;  // optional output of the merged result (NULL: none)
+  int final_bf16;
+  int B, H, S, d;
+  int64_t as[3], ps[3], fs[3];
+};
+cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st);
+// o = 0, lse = -inf for every row (attention over an empty key set).
+cudaError_t launch_fill_empty(void* o, int out_bf16, float* lse, int B, int H, int S, int d, const int64_t os[3],
+                              cudaStream_t st);
 
 }  // namespace yr

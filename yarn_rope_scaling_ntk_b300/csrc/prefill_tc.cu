@@ -58,7 +58,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct TcParams {
-  int B, Hq, Hkv, S, group, n_pairs;
+  int B, Hq, Hkv, group, n_pairs;
+  int Sq, Skv, qp0, kp0;  // query rows, keys, position of query row 0 / key 0
   int kv_per_sched;  // KV heads per scheduling group (see the CTA order below)
   int mask, sink, window, ring_blocks, cs;
   float scale_log2;
@@ -78,34 +79,42 @@ struct TcParams {
 // range [0, last] minus at most one gap [gap_lo, gap_hi) (chunks between the
 // sinks and the start of the window), so the walk is a few compares per chunk.
 struct Walk {
-  int N, cpb, cs, mask, sink, window;
-  int r0a, r1a, r0b, r1b;
+  int N, cpb, cs, mask, sink, window, qp0, kp0;
+  int r0a, r1a, r0b, r1b;  // local query rows of tiles a and b
   bool hasa, hasb;
   int last, gap_lo, gap_hi, I;
   int t, c, c_end, rb;  // ring step, chunk, end of the block's visible chunks, block
   __device__ void init(const TcParams& p, int pair) {
     cs = p.cs;
     N = p.ring_blocks;
-    const int n_chunks = (p.S + cs - 1) / cs;
-    const int bs = N > 1 ? p.S / N : 0;
+    const int n_chunks = (p.Skv + cs - 1) / cs;
+    const int bs = N > 1 ? p.Skv / N : 0;  // ring blocks only when Sq == Skv and both start at 0
     cpb = N > 1 ? bs / cs : n_chunks;
     r0a = pair * 2 * BM;
     r0b = r0a + BM;
-    hasa = r0a < p.S;
-    hasb = r0b < p.S;
-    r1a = min(p.S, r0a + BM) - 1;
-    r1b = min(p.S, r0b + BM) - 1;
+    hasa = r0a < p.Sq;
+    hasb = r0b < p.Sq;
+    r1a = min(p.Sq, r0a + BM) - 1;
+    r1b = min(p.Sq, r0b + BM) - 1;
+    qp0 = p.qp0;
+    kp0 = p.kp0;
     const int lim = hasb ? r1b : r1a;
     mask = p.mask;
     sink = p.sink;
     window = p.window;
-    last = mask == YR_MASK_NONE ? n_chunks - 1 : min(n_chunks - 1, lim / cs);
+    // positions: query row r sits at qp0 + r, key n at kp0 + n
+    if (mask == YR_MASK_NONE) {
+      last = n_chunks - 1;
+    } else {
+      const int reach = qp0 + lim - kp0;  // the last key index any row sees
+      last = reach < 0 ? -1 : min(n_chunks - 1, reach / cs);
+    }
     gap_lo = gap_hi = 0;
     if (mask == YR_MASK_SINK_WINDOW) {
-      // chunks with a sink: c * cs < sink; chunks that reach the window of
-      // row r0a: c * cs + cs - 1 > r0a - window
-      const int sink_chunks = (sink + cs - 1) / cs;
-      const int x = r0a - window - cs + 1;
+      // chunks with a sink: kp0 + c * cs < sink; chunks that reach the window
+      // of row r0a: kp0 + c * cs + cs - 1 > qp0 + r0a - window
+      const int sink_chunks = sink > kp0 ? (sink - kp0 + cs - 1) / cs : 0;
+      const int x = qp0 + r0a - window - cs + 1 - kp0;
       const int w_lo = x < 0 ? 0 : x / cs + 1;
       if (sink_chunks < w_lo) { gap_lo = sink_chunks; gap_hi = w_lo; }
     }
@@ -115,8 +124,9 @@ struct Walk {
     rb = 0;
   }
   __device__ __forceinline__ bool visible(bool has, int r0, int r1, int n0) const {
-    const bool in_window = (mask != YR_MASK_SINK_WINDOW) | (n0 < sink) | (n0 + cs - 1 > r0 - window);
-    return has & ((mask == YR_MASK_NONE) | ((n0 <= r1) & in_window));
+    const int ng = kp0 + n0, r0g = qp0 + r0, r1g = qp0 + r1;
+    const bool in_window = (mask != YR_MASK_SINK_WINDOW) | (ng < sink) | (ng + cs - 1 > r0g - window);
+    return has & ((mask == YR_MASK_NONE) | ((ng <= r1g) & in_window));
   }
   // next chunk start seen by either tile (or -1), with per-tile visibility
   __device__ __forceinline__ int next(bool& v0, bool& v1) {
@@ -143,8 +153,9 @@ struct Walk {
 
 // does a tile with rows [r0, r1] need the per-element mask on chunk n0?
 __device__ __forceinline__ bool needs_mask(const TcParams& p, int r0, int r1, int n0) {
-  return p.cs < BN || n0 + BN > p.S || (p.mask != YR_MASK_NONE && n0 + BN - 1 > r0) ||
-         (p.mask == YR_MASK_SINK_WINDOW && n0 <= r1 - p.window);
+  const int ng = p.kp0 + n0, r0g = p.qp0 + r0, r1g = p.qp0 + r1;
+  return p.cs < BN || n0 + BN > p.Skv || (p.mask != YR_MASK_NONE && ng + BN - 1 > r0g) ||
+         (p.mask == YR_MASK_SINK_WINDOW && ng <= r1g - p.window);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -412,11 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (needs_mask(p, my_r0, my_r1, n0)) {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
-          const int n = n0 + e;
-          bool vis = e < p.cs && n < p.S;
+          const int n = n0 + e;                           // local key index
+          bool vis = e < p.cs && n < p.Skv;
           if (p.mask != YR_MASK_NONE) {
-            vis = vis && n <= m;
-            if (p.mask == YR_MASK_SINK_WINDOW) vis = vis && (n < p.sink || m - n < p.window);
+            const int ng = p.kp0 + n, mg = p.qp0 + m;    // positions
+            vis = vis && ng <= mg;
+            if (p.mask == YR_MASK_SINK_WINDOW) vis = vis && (ng < p.sink || mg - ng < p.window);
           }
           if (!vis) x[e] = -INFINITY;
         }
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (have) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const bool row_ok = m < p.S;
+        const bool row_ok = m < p.Sq;
         char* orow = static_cast<char*>(p.o) +
                      (b * p.os[0] + hq * p.os[1] + (int64_t)m * p.os[2]) * (p.out_bf16 ? 2 : 4);
 #pragma unroll
@@ -519,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (p.lse && row_ok)
-          p.lse[((int64_t)b * p.Hq + hq) * p.S + m] =
+          p.lse[((int64_t)b * p.Hq + hq) * p.Sq + m] =
               l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       }
     }
@@ -576,13 +588,14 @@ bool make_map(CUtensorMap* map, const void* base, int B, int H, int S, int D, co
 template <int D>
 cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.B, a.Hq, a.S, D, a.qs) || !make_map(&mk, a.k, a.B, a.Hkv, a.S, D, a.ks) ||
-      !make_map(&mv, a.v, a.B, a.Hkv, a.S, D, a.vs))
+  if (!make_map(&mq, a.q, a.B, a.Hq, a.Sq, D, a.qs) || !make_map(&mk, a.k, a.B, a.Hkv, a.Skv, D, a.ks) ||
+      !make_map(&mv, a.v, a.B, a.Hkv, a.Skv, D, a.vs))
     return cudaErrorInvalidValue;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.S = a.S; p.group = a.Hq / a.Hkv;
-  p.n_pairs = (a.S + 2 * BM - 1) / (2 * BM);
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.group = a.Hq / a.Hkv;
+  p.Sq = a.Sq; p.Skv = a.Skv; p.qp0 = a.q_pos0; p.kp0 = a.k_pos0;
+  p.n_pairs = (a.Sq + 2 * BM - 1) / (2 * BM);
   {
     // enough KV heads per scheduling group for about three waves of CTAs
     const int per_kv = p.n_pairs * p.group;
@@ -591,7 +604,7 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
     p.kv_per_sched = k < 1 ? 1 : (k > n_kv ? n_kv : k);
   }
   p.mask = a.mask; p.sink = a.sink; p.window = a.window; p.ring_blocks = a.ring_blocks;
-  p.cs = (a.ring_blocks > 1 && (a.S / a.ring_blocks) % BN != 0) ? 64 : BN;
+  p.cs = (a.ring_blocks > 1 && (a.Skv / a.ring_blocks) % BN != 0) ? 64 : BN;
   p.scale_log2 = a.scale_log2;
   p.o = a.o;
   for (int i = 0; i < 3; ++i) p.os[i] = a.os[i];
@@ -611,7 +624,9 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t st) {
-  if (a.ring_blocks > 1 && (a.S / a.ring_blocks) % 64 != 0) return cudaErrorInvalidValue;
+  if (a.ring_blocks > 1 &&
+      (a.Sq != a.Skv || a.q_pos0 != 0 || a.k_pos0 != 0 || (a.Skv / a.ring_blocks) % 64 != 0))
+    return cudaErrorInvalidValue;
   return a.d == 128 ? launch_d<128>(a, st) : launch_d<64>(a, st);
 }
 
