@@ -387,6 +387,17 @@ def run_ours(args):
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     del kc, vc
 
+    # ---- the same decode over an FP8 E4M3 cache (half the bytes) ----------
+    fq, fkc, fvc, fks, fvs, fnv, frs = W.decode_inputs_fp8(wd, dev)
+    dec8 = lambda: api.attn_fwd_decode_sinkwindow_fp8(dcfg, fq, fkc, fvc, fks, fvs, fnv, frs, wd.sink,
+                                                       wd.window, out=do, workspace=dws)
+    for _ in range(3):
+        dec8()
+    dec8_ms = statistics.mean(timed(dec8, max(10, args.steps), stream))
+    dec8_bytes = 2 * fkc.numel() + 2 * 4 * fks.numel() + fq.numel() * 2 + do.numel() * 2 + 2 * 4 * wd.B
+    dec8_gbs = dec8_bytes / (dec8_ms * 1e-3) / 1e9
+    del fkc, fvc
+
     # ---- standalone rope_apply on Q and K of the prefill workload ---------
     def rope_qk():
         api.rope_apply(cfg, q, out=o)
@@ -429,11 +440,15 @@ def run_ours(args):
                      "kernel_ms": attn_ms, "peak_kind": f"bf16 burst ({peak_src}; kernel timed alone)",
                      "frac_of_sustained": attn_tflops / tf_sust},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps,  # per step: rotation of Q, rotation of K, attention
         "clocks": cs,
         "decode": {"workload": wd.name, "value": dec_gbs, "unit": "GB/s", "ms": dec_ms,
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                                 "frac": dec_gbs / hbm, "traffic": traffic("decode")}},
+        "decode_fp8": {"workload": wd.name + "_fp8_e4m3", "value": dec8_gbs, "unit": "GB/s", "ms": dec8_ms,
+                       "speedup_vs_bf16_cache": dec_ms / dec8_ms,
+                       "roofline": {"bound": "hbm", "achieved": dec8_gbs, "peak": hbm, "unit": "GB/s",
+                                    "frac": dec8_gbs / hbm, "traffic": None}},
         "other_prefill_workloads": others,
         "rope_apply": {"workload": "Q and K of " + w.name, "value": rope_gbs, "unit": "GB/s",
                        "ms": rope_ms,

@@ -259,6 +259,22 @@ yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, cons
                                      void* o, float* lse, int32_t num_splits, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* attn_fwd_decode_sinkwindow over an FP8 cache: k_cache and v_cache hold
+ * OCP FP8 E4M3 values (1 byte each, [B, Hkv, sink + window, d]) and the
+ * dequantised entry is the stored value times the float32 scale of its
+ * (sequence, KV head): k_scale[b * Hkv + h] for keys, v_scale[...] for
+ * values (device arrays of B * Hkv).  Quantising the cache to FP8 halves the
+ * bytes the memory-bound decode reads ("Context Window Scaling ...", FAQ 3:
+ * KV-cache quantisation to FP8 or INT4).  Keys are stored unrotated; the
+ * rotation, mask, positions, splits, workspace and outputs are those of
+ * attn_fwd_decode_sinkwindow (q and o stay bfloat16). */
+yr_status attn_fwd_decode_sinkwindow_fp8(const yr_rope_cfg* cfg, const void* q, const void* k_cache,
+                                         const void* v_cache, const float* k_scale, const float* v_scale,
+                                         const int32_t* n_valid, const int32_t* ring_start, int32_t B,
+                                         int32_t Hq, int32_t Hkv, int32_t d, int32_t sink, int32_t window,
+                                         void* o, float* lse, int32_t num_splits, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* attn_fwd_decode_sinkwindow without a workspace argument, for callers that
  * cannot allocate device memory when they call (for example an engine's
  * per-step hook that must not allocate, or a process whose device memory is

@@ -106,6 +106,8 @@ def load_library():
         "yr_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
         "attn_fwd_decode_sinkwindow": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
                                              I32, _P, _P, I32, _P, SZ, _P]),
+        "attn_fwd_decode_sinkwindow_fp8": (I32, [cfgp, _P, _P, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
+                                                 I32, _P, _P, I32, _P, SZ, _P]),
         "attn_fwd_decode_sinkwindow_noalloc": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32,
                                                      I32, I32, _P, _P, I32, _P]),
         "yr_sync_status": (I32, [_P]),
@@ -290,6 +292,41 @@ def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ri
     _check(lib.attn_fwd_decode_sinkwindow(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(n_valid), _ptr(ring_start),
         B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return (o, lse) if return_lse else o
+
+
+def attn_fwd_decode_sinkwindow_fp8(cfg: RopeConfig, q, k_cache, v_cache, k_scale, v_scale, n_valid,
+                                   ring_start, sink: int, window: int, num_splits: int = 0, out=None,
+                                   lse=None, return_lse: bool = False, workspace=None, stream=None):
+    """Decode over an FP8 E4M3 cache: k_cache / v_cache [B, Hkv, sink + window,
+    d] (torch.float8_e4m3fn or uint8 bytes), k_scale / v_scale float32
+    [B, Hkv]; q [B, Hq, d] bfloat16.  Returns o (and lse)."""
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bfloat16")
+    for t in (k_cache, v_cache):
+        if t.element_size() != 1 or not t.is_contiguous() or t.shape != (B, Hkv, sink + window, d):
+            raise ValueError("caches must be contiguous 1-byte [B, Hkv, sink + window, d]")
+    for t in (k_scale, v_scale):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != B * Hkv:
+            raise ValueError("scales must be contiguous float32 [B, Hkv]")
+    for t in (n_valid, ring_start):
+        if t.dtype != torch.int32 or t.shape != (B,):
+            raise ValueError("n_valid and ring_start must be int32 [B]")
+    o = torch.empty_like(q) if out is None else out
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    c = cfg.c()
+    _check(lib.attn_fwd_decode_sinkwindow_fp8(
+        ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(n_valid),
+        _ptr(ring_start), B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits),
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return (o, lse) if return_lse else o

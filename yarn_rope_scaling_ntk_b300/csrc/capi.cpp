@@ -380,14 +380,12 @@ size_t yr_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, 
   return (size_t)splits * B * Hq * (d + 2) * sizeof(float);
 }
 
-yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, const void* k_cache,
-                                     const void* v_cache, const int32_t* n_valid,
-                                     const int32_t* ring_start, int32_t B, int32_t Hq,
-                                     int32_t Hkv, int32_t d, int32_t sink, int32_t window,
-                                     void* o, float* lse, int32_t num_splits, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
-  clear_error();
-  if (!cfg) return fail(YR_ERR_INVALID_ARG, "cfg is NULL");
+static yr_status decode_impl(const char* who, const yr_rope_cfg* cfg, const void* q, const void* k_cache,
+                             const void* v_cache, int fp8, const float* k_scale, const float* v_scale,
+                             const int32_t* n_valid, const int32_t* ring_start, int32_t B, int32_t Hq,
+                             int32_t Hkv, int32_t d, int32_t sink, int32_t window, void* o, float* lse,
+                             int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!cfg) return fail(YR_ERR_INVALID_ARG, "%s: cfg is NULL", who);
   if (B < 0 || Hq < 0 || Hkv < 0) return fail(YR_ERR_INVALID_ARG, "negative shape");
   if (d != 64 && d != 128) return fail(YR_ERR_UNSUPPORTED, "decode head dimension %d (64 or 128)", d);
   if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return fail(YR_ERR_INVALID_ARG, "Hq %% Hkv != 0");
@@ -403,6 +401,7 @@ yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, cons
   if (B == 0) return YR_OK;
   if (!q || !k_cache || !v_cache || !n_valid || !ring_start || !o)
     return fail(YR_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (fp8 && (!k_scale || !v_scale)) return fail(YR_ERR_INVALID_ARG, "%s: k_scale and v_scale are required", who);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
     return fail(YR_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   const int splits = num_splits > 0 ? num_splits : yr_decode_auto_splits(B, Hkv, sink, window);
@@ -414,10 +413,35 @@ yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, cons
   memset(&a, 0, sizeof(a));
   a.q = q; a.kc = k_cache; a.vc = v_cache; a.n_valid = n_valid; a.ring_start = ring_start;
   a.o = o; a.lse = lse; a.ws = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.k_scale = k_scale; a.v_scale = v_scale; a.fp8 = fp8;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.sink = sink; a.window = window; a.splits = splits;
   a.scale_log2 = (float)(ms * ms / sqrt((double)d) * 1.4426950408889634073599246810019);
   cudaError_t e = launch_decode(a, f, as_stream(stream));
-  return e == cudaSuccess ? YR_OK : cuda_fail(e, "attn_fwd_decode_sinkwindow launch");
+  return e == cudaSuccess ? YR_OK : cuda_fail(e, "decode launch");
+}
+
+yr_status attn_fwd_decode_sinkwindow(const yr_rope_cfg* cfg, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* n_valid,
+                                     const int32_t* ring_start, int32_t B, int32_t Hq,
+                                     int32_t Hkv, int32_t d, int32_t sink, int32_t window,
+                                     void* o, float* lse, int32_t num_splits, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  clear_error();
+  return decode_impl("attn_fwd_decode_sinkwindow", cfg, q, k_cache, v_cache, 0, nullptr, nullptr, n_valid,
+                     ring_start, B, Hq, Hkv, d, sink, window, o, lse, num_splits, workspace, workspace_bytes,
+                     stream);
+}
+
+yr_status attn_fwd_decode_sinkwindow_fp8(const yr_rope_cfg* cfg, const void* q, const void* k_cache,
+                                         const void* v_cache, const float* k_scale, const float* v_scale,
+                                         const int32_t* n_valid, const int32_t* ring_start, int32_t B,
+                                         int32_t Hq, int32_t Hkv, int32_t d, int32_t sink, int32_t window,
+                                         void* o, float* lse, int32_t num_splits, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  clear_error();
+  return decode_impl("attn_fwd_decode_sinkwindow_fp8", cfg, q, k_cache, v_cache, 1, k_scale, v_scale, n_valid,
+                     ring_start, B, Hq, Hkv, d, sink, window, o, lse, num_splits, workspace, workspace_bytes,
+                     stream);
 }
 
 yr_status yr_sync_status(void* stream) {

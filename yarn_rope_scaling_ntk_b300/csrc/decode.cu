@@ -16,6 +16,7 @@
 // sum, unnormalised output) whose reference max moves lazily.  States are
 // merged across the warp by shuffles, across warps in shared memory, and
 // across slices by a second kernel.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -41,14 +42,16 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
 // PPT rotation pairs per thread: 8 (two 16-byte vectors per key row) when
 // one query head shares the key, 4 when several do, so the per-thread query and
-// accumulator state fits the registers of nine resident warps.
-template <int D, int PPT>
+// accumulator state fits the registers of nine resident warps.  EB is the
+// byte size of a cache element (2: bfloat16, 1: FP8 E4M3); a chunk holds the
+// same bytes either way, so an FP8 chunk holds twice the keys.
+template <int D, int PPT, int EB>
 struct DecodeShape {
   static constexpr int TPK = D / 2 / PPT;     // threads per key
   static constexpr int KPW = 32 / TPK;        // keys per warp step
   static constexpr int KPS = KPW * kWarps;    // keys per CTA step
-  static constexpr int CK = 2 * KPS;          // keys per chunk (2 per thread)
-  static constexpr int ROW = D * 2;           // bytes per cache row
+  static constexpr int CK = (4 / EB) * KPS;   // keys per chunk
+  static constexpr int ROW = D * EB;          // bytes per cache row
   static constexpr int STAGE = CK * ROW;      // bytes of K (or V) per stage
   static constexpr int SMEM = 2 * NSTG * STAGE;
 };
@@ -71,6 +74,33 @@ __device__ __forceinline__ void load_bf16(const uint8_t* p, float (&x)[N]) {
   }
 }
 
+// N consecutive FP8 E4M3 values (N = 8 or 4) to float, through the hardware
+// pair conversion to half precision (exact: every E4M3 value is a half).
+template <int N>
+__device__ __forceinline__ void load_e4m3(const uint8_t* p, float (&x)[N]) {
+  uint32_t w[N / 4];
+  if constexpr (N == 8) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    w[0] = u.x; w[1] = u.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+    const __half2 h2 = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
+    const float2 f2 = __half22float2(h2);
+    x[2 * k] = f2.x;
+    x[2 * k + 1] = f2.y;
+  }
+}
+
+template <int N, int EB>
+__device__ __forceinline__ void load_cache(const uint8_t* p, float (&x)[N]) {
+  if constexpr (EB == 2) load_bf16<N>(p, x);
+  else load_e4m3<N>(p, x);
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -79,10 +109,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(DecodeLaunch a, RopeFreqs f) {
   constexpr int PPT = G >= 2 ? 4 : 8;
-  using Sh = DecodeShape<D, PPT>;
+  constexpr int QROW = D * 2;  // the query is bfloat16
+  using Sh = DecodeShape<D, PPT, EB>;
   constexpr int TPK = Sh::TPK, KPW = Sh::KPW, KPS = Sh::KPS, CK = Sh::CK, ROW = Sh::ROW;
   constexpr int HALF = D / 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -177,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const uint8_t* qp = static_cast<const uint8_t*>(a.q) + ((int64_t)b * a.Hq + hq0 + g) * ROW;
+      const uint8_t* qp = static_cast<const uint8_t*>(a.q) + ((int64_t)b * a.Hq + hq0 + g) * QROW;
       float x1[PPT], x2[PPT];
       load_bf16<PPT>(qp + c8 * PPT * 2, x1);
       load_bf16<PPT>(qp + HALF * 2 + c8 * PPT * 2, x2);
@@ -188,6 +219,12 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       }
     }
   }
+
+  // FP8 caches: dequantised value = stored value x scale of the (sequence,
+  // KV head).  The rotation is linear, so the key scale multiplies each dot
+  // product and the value scale the output.
+  const float k_scale = EB == 1 ? a.k_scale[bh] : 1.f;
+  const float v_scale = EB == 1 ? a.v_scale[bh] : 1.f;
 
   float mrun[G], lrun[G], acc1[G][PPT], acc2[G][PPT];
 #pragma unroll
@@ -211,13 +248,13 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       const int kk = u * KPS + warp * KPW + kg;  // key within the chunk
       const int j = jc + kk;
       const bool valid = j < j1;
-      const uint8_t* kr = stK + kk * ROW + c8 * PPT * 2;
-      const uint8_t* vr = stV + kk * ROW + c8 * PPT * 2;
+      const uint8_t* kr = stK + kk * ROW + c8 * PPT * EB;
+      const uint8_t* vr = stV + kk * ROW + c8 * PPT * EB;
       float x1[PPT], x2[PPT], y1[PPT], y2[PPT];
-      load_bf16<PPT>(kr, x1);
-      load_bf16<PPT>(kr + HALF * 2, x2);
-      load_bf16<PPT>(vr, y1);
-      load_bf16<PPT>(vr + HALF * 2, y2);
+      load_cache<PPT, EB>(kr, x1);
+      load_cache<PPT, EB>(kr + HALF * EB, x2);
+      load_cache<PPT, EB>(vr, y1);
+      load_cache<PPT, EB>(vr + HALF * EB, y2);
       float kr1[PPT], kr2[PPT];
 #pragma unroll
       for (int k = 0; k < PPT; ++k) {
@@ -233,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
         for (int k = 0; k < PPT; ++k) dot = fmaf(q1[g][k], kr1[k], fmaf(q2[g][k], kr2[k], dot));
 #pragma unroll
         for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (EB == 1) dot *= k_scale;
         if (valid) {
           if (dot > mrun[g] + kRescaleThreshold) {  // lazy: the reference moves rarely
             const float corr = exp2_diff(mrun[g], dot);
@@ -310,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       L += s_ml[(w * G + g) * 2 + 1] * wt;
       O += s_acc[(w * G + g) * D + dim] * wt;
     }
+    O *= v_scale;
     const int64_t bhq = (int64_t)b * a.Hq + hq0 + g;
     if (a.splits == 1) {
       const float out = L > 0.f ? O / L : 0.f;
@@ -348,14 +387,14 @@ __global__ void decode_merge_kernel(DecodeLaunch a) {
   }
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 cudaError_t launch_dg(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int groups = (a.Hq / a.Hkv) / G;
   dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)a.splits, (unsigned)groups);
-  const int smem = DecodeShape<D, (G >= 2 ? 4 : 8)>::SMEM;
-  cudaError_t e0 = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = DecodeShape<D, (G >= 2 ? 4 : 8), EB>::SMEM;
+  cudaError_t e0 = cudaFuncSetAttribute(decode_kernel<D, G, EB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e0 != cudaSuccess) return e0;
-  decode_kernel<D, G><<<grid, kThreads, smem, st>>>(a, f);
+  decode_kernel<D, G, EB><<<grid, kThreads, smem, st>>>(a, f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   decode_merge_kernel<<<(unsigned)(a.B * a.Hq), 128, 0, st>>>(a);
@@ -369,14 +408,24 @@ cudaError_t launch_decode(const DecodeLaunch& a_in, const RopeFreqs& f, cudaStre
   a.status = device_status_word();
   if (!a.status) return cudaErrorInvalidValue;
   const int G = a.Hq / a.Hkv;
-  if (a.d == 128) {
-    if (G == 1) return launch_dg<128, 1>(a, f, st);
-    if (G == 2) return launch_dg<128, 2>(a, f, st);
-    return launch_dg<128, 4>(a, f, st);  // G = 4 or 8 (two head groups)
+  if (a.fp8) {
+    if (a.d == 128) {
+      if (G == 1) return launch_dg<128, 1, 1>(a, f, st);
+      if (G == 2) return launch_dg<128, 2, 1>(a, f, st);
+      return launch_dg<128, 4, 1>(a, f, st);
+    }
+    if (G == 1) return launch_dg<64, 1, 1>(a, f, st);
+    if (G == 2) return launch_dg<64, 2, 1>(a, f, st);
+    return launch_dg<64, 4, 1>(a, f, st);
   }
-  if (G == 1) return launch_dg<64, 1>(a, f, st);
-  if (G == 2) return launch_dg<64, 2>(a, f, st);
-  return launch_dg<64, 4>(a, f, st);
+  if (a.d == 128) {
+    if (G == 1) return launch_dg<128, 1, 2>(a, f, st);
+    if (G == 2) return launch_dg<128, 2, 2>(a, f, st);
+    return launch_dg<128, 4, 2>(a, f, st);  // G = 4 or 8 (two head groups)
+  }
+  if (G == 1) return launch_dg<64, 1, 2>(a, f, st);
+  if (G == 2) return launch_dg<64, 2, 2>(a, f, st);
+  return launch_dg<64, 4, 2>(a, f, st);
 }
 
 }  // namespace yr

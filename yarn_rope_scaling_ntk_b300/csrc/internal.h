@@ -58,6 +58,9 @@ struct DecodeLaunch {
   void* o;
   float* lse;
   float* ws;  // split partials (NULL when splits == 1)
+  const float* k_scale;  // FP8 caches: per (sequence, KV head) scales
+  const float* v_scale;
+  int fp8;               // 1: caches are FP8 E4M3, 0: bfloat16
   int B, Hq, Hkv, d, sink, window, splits;
   float scale_log2;
   int* status;  // device status word (set by the launcher)

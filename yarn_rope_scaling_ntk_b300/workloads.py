@@ -122,3 +122,29 @@ def sample_rows(S: int, count: int, index: int, extra=()):
     r = torch.randint(0, S, (count,), generator=g)
     forced = torch.tensor([x for x in (0, 1, 127, 128, 129, S - 1, *extra) if 0 <= x < S])
     return torch.unique(torch.cat([r, forced]))
+
+
+def decode_inputs_fp8(w: Decode, device="cpu", seed_index: int | None = None):
+    """The decode inputs with the caches stored as FP8 E4M3: K and V drawn
+    N(0, 1) as in ``decode_inputs``, then each (sequence, KV head) stored as
+    E4M3 bytes of x / scale with scale = max|x| / 448 (the largest E4M3
+    magnitude).  Returns q (bf16), k_codes, v_codes (uint8), k_scale,
+    v_scale (float32 [B, Hkv]), n_valid, ring_start."""
+    g = generator(w.index if seed_index is None else seed_index, device)
+    C = w.sink + w.window
+    q = torch.randn(w.B, w.Hq, w.d, generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn(w.B, w.Hkv, C, w.d, generator=g, device=device)
+    v = torch.randn(w.B, w.Hkv, C, w.d, generator=g, device=device)
+    ring_start = torch.randint(0, max(w.window, 1), (w.B,), generator=g, device=device, dtype=torch.int32)
+    if w.full:
+        n_valid = torch.full((w.B,), C, dtype=torch.int32, device=device)
+    else:
+        n_valid = torch.randint(1, C + 1, (w.B,), generator=g, device=device, dtype=torch.int32)
+    out = []
+    for x in (k, v):
+        scale = (x.abs().amax(dim=(2, 3)) / 448.0).clamp_min(1e-12)
+        codes = (x / scale[:, :, None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        out += [codes.contiguous(), scale.float().contiguous()]
+        del x
+    kc, ks, vc, vs = out
+    return q, kc, vc, ks, vs, n_valid, ring_start
