@@ -195,16 +195,36 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
   for (int k = 0; k < PPT; ++k) fr[k] = f.f[c8 * PPT + k];
   const bool identity = f.identity != 0;
 
-  // Rotated query at position n - 1, pre-multiplied by scale * log2(e) so
-  // that the dot product is the logit in base-2 units.
-  float q1[G][PPT], q2[G][PPT];
+  // The logit of key position j is <R_m q, R_j k> = <R_(m-j) q, k> with m =
+  // n - 1 the query position ("Context Window Scaling ...", Section 2: the
+  // inner product depends only on the displacement).  A thread visits its
+  // keys at j, j + KPS, j + 2 KPS, ..., so the rotation advances by the fixed
+  // angle KPS theta_i per step: one complex multiply per pair, re-anchored
+  // exactly (integer displacement, exact turn reduction) at every chunk.
+  //  G == 1: the query is rotated backwards, q_hat = R_(m-j) q, and dotted
+  //          with the raw key (no per-key rotation of K).
+  //  G  > 1: the G query heads share the key, so the key's cos/sin advance
+  //          instead and K is rotated once for all of them.
+  // The recurrence is used for FP8 caches, where the halved bytes leave the
+  // kernel bound by this arithmetic.  For bfloat16 caches the kernel is
+  // bound by HBM, and an exact per-key angle keeps consecutive keys
+  // independent (more instruction-level parallelism at the same bytes).
+  constexpr bool kRecur = EB == 1;
+  constexpr bool kRotQ = kRecur && G == 1;
+  const int mq = n > 0 ? n - 1 : 0;
+  float q1[G][PPT], q2[G][PPT];   // scaled query: raw (kRotQ) or rotated at m
+  float stc[PPT], sts[PPT];       // cos / sin of the step angle KPS theta_i
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    if (identity) { stc[k] = 1.f; sts[k] = 0.f; }
+    else turn_cos_sin<false>((float)KPS, fr[k], stc[k], sts[k]);
+  }
   {
     float cs[PPT], sn[PPT];
-    const float mq = (float)(n > 0 ? n - 1 : 0);
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-      if (identity) { cs[k] = 1.f; sn[k] = 0.f; }
-      else turn_cos_sin<false>(mq, fr[k], cs[k], sn[k]);
+      if (identity || kRotQ) { cs[k] = 1.f; sn[k] = 0.f; }
+      else turn_cos_sin<false>((float)mq, fr[k], cs[k], sn[k]);
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -243,6 +263,21 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
     if (!ok) break;
     const uint8_t* stK = sK + s * Sh::STAGE;
     const uint8_t* stV = sV + s * Sh::STAGE;
+    // anchor of this chunk: the rotation for the thread's first key j_a
+    const int j_a = jc + warp * KPW + kg;
+    float rc[PPT], rs_[PPT];  // cos / sin of (m - j) theta (kRotQ) or j theta
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      if (identity || !kRecur) { rc[k] = 1.f; rs_[k] = 0.f; }
+      else turn_cos_sin<false>((float)(kRotQ ? mq - j_a : j_a), fr[k], rc[k], rs_[k]);
+    }
+    // kRotQ: the backward-rotated query itself is the recurrence state
+    float qh1[PPT], qh2[PPT];
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      qh1[k] = q1[0][k] * rc[k] - q2[0][k] * rs_[k];
+      qh2[k] = q1[0][k] * rs_[k] + q2[0][k] * rc[k];
+    }
 #pragma unroll
     for (int u = 0; u < CK / KPS; ++u) {
       const int kk = u * KPS + warp * KPW + kg;  // key within the chunk
@@ -255,19 +290,42 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       load_cache<PPT, EB>(kr + HALF * EB, x2);
       load_cache<PPT, EB>(vr, y1);
       load_cache<PPT, EB>(vr + HALF * EB, y2);
-      float kr1[PPT], kr2[PPT];
+      float kr1[PPT], kr2[PPT];   // key as dotted: raw (kRotQ) or rotated at j
+      float qa1[G][PPT], qa2[G][PPT];
+      if (!kRecur && !identity) {
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) turn_cos_sin<false>((float)j, fr[k], rc[k], rs_[k]);
+      }
 #pragma unroll
       for (int k = 0; k < PPT; ++k) {
-        float cs = 1.f, sn = 0.f;
-        if (!identity) turn_cos_sin<false>((float)j, fr[k], cs, sn);
-        kr1[k] = x1[k] * cs - x2[k] * sn;
-        kr2[k] = x1[k] * sn + x2[k] * cs;
+        if (kRotQ) {
+          kr1[k] = x1[k];
+          kr2[k] = x2[k];
+          qa1[0][k] = qh1[k];
+          qa2[0][k] = qh2[k];
+          // next key: q_hat <- R(-KPS theta) q_hat
+          const float a1 = qh1[k], a2 = qh2[k];
+          qh1[k] = a1 * stc[k] + a2 * sts[k];
+          qh2[k] = a2 * stc[k] - a1 * sts[k];
+        } else {
+          kr1[k] = x1[k] * rc[k] - x2[k] * rs_[k];
+          kr2[k] = x1[k] * rs_[k] + x2[k] * rc[k];
+#pragma unroll
+          for (int g = 0; g < G; ++g) { qa1[g][k] = q1[g][k]; qa2[g][k] = q2[g][k]; }
+        }
+        // advance to the thread's next key: (m - j) decreases (kRotQ) or j
+        // increases by KPS
+        if (kRecur && !kRotQ) {
+          const float c0 = rc[k], s0 = rs_[k];
+          rc[k] = c0 * stc[k] - s0 * sts[k];
+          rs_[k] = s0 * stc[k] + c0 * sts[k];
+        }
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float dot = 0.f;
 #pragma unroll
-        for (int k = 0; k < PPT; ++k) dot = fmaf(q1[g][k], kr1[k], fmaf(q2[g][k], kr2[k], dot));
+        for (int k = 0; k < PPT; ++k) dot = fmaf(qa1[g][k], kr1[k], fmaf(qa2[g][k], kr2[k], dot));
 #pragma unroll
         for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
         if (EB == 1) dot *= k_scale;
