@@ -223,6 +223,35 @@ yr_status attn_merge_partial(float* o_acc, float* lse_acc, const float* o_part, 
                              const int64_t acc_strides[3], const int64_t part_strides[3],
                              const int64_t final_strides[3], void* stream);
 
+/* Bytes of device workspace attn_bwd needs. */
+size_t yr_bwd_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t S, int32_t d);
+
+/* Gradients of attn_fwd_prefill (natural order, positions 0 .. S - 1) with
+ * respect to the unrotated q, k and v, for the fine-tuning that the context
+ * extension methods rely on ("Context Window Scaling ...", Section 3:
+ * YaRN's brief fine-tune; "Context Length Extension", Position
+ * Interpolation: ~1000 fine-tuning steps).  With P the softmax of
+ * scale * <R_m q_m, R_n k_n>, dO the gradient of the output and
+ * D_m = sum_c dO[m, c] O[m, c]:
+ *   dv = P^T dO,  dS = P * (dO V^T - D),
+ *   dq = scale R_m^T (dS Kr),  dk = scale R_n^T (dS^T Qr).
+ * q, o, dout : device [B, Hq, S, d] in_dtype;  k, v : [B, Hkv, S, d].
+ * lse  : device float32 [B, Hq, S] contiguous, the forward's row log-sum-exp.
+ * dq   : device [B, Hq, S, d];  dk, dv : [B, Hkv, S, d], out_dtype (F32 or
+ *        BF16).  GQA: dk and dv sum over the query heads of their group.
+ * Supported: d in {64, 128}, S a multiple of 128.  mask, sink, window and
+ * softmax_scale as in attn_fwd_prefill.  The products run on bfloat16
+ * operands (the rotated q and k, v, dO, P and dS) with float32 accumulation.
+ * workspace: device scratch of yr_bwd_workspace_bytes(). */
+yr_status attn_bwd(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v, const void* o,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int32_t in_dtype,
+                   int32_t out_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
+                   const int64_t q_strides[3], const int64_t k_strides[3], const int64_t v_strides[3],
+                   const int64_t o_strides[3], const int64_t do_strides[3], const int64_t dq_strides[3],
+                   const int64_t dk_strides[3], const int64_t dv_strides[3], int32_t mask, int32_t sink,
+                   int32_t window, float softmax_scale, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Split count the decode entry point uses when num_splits <= 0. */
 int32_t yr_decode_auto_splits(int32_t B, int32_t Hkv, int32_t sink, int32_t window);
 

@@ -197,3 +197,45 @@ def decode_head(q, k_cache, v_cache, n_valid, ring_start, sink, window, theta, s
     qr = _rope.rotate(np.asarray(q, dtype=np.float64)[None, :], np.array([n_valid - 1]), theta)
     o, lse = attention_rows(qr, np.array([n_valid - 1]), k, vv, "none", 0, 0, scale)
     return o[0], lse[0]
+
+
+def backward_head(q, k, v, do, q_pos, k_pos, theta, scale, mask, sink=0, window=0):
+    """Gradients of L = sum(O * dO) for one (batch, head) of
+    O = softmax(scale * <R_m q_m, R_n k_n>) V over visible keys, by the chain
+    rule written out (the derivative of the softmax attention the pages
+    define in "Context Window Scaling ...", Section 1, with the rotation of
+    Section 2 applied to q and k):
+
+        P = softmax rows of scale * Qr Kr^T (Qr, Kr the rotated q, k)
+        dV = P^T dO;  dP = dO V^T;  D_m = sum_n P_mn dP_mn (= rowsum dO * O)
+        dS = P * (dP - D);  dQr = scale dS Kr;  dKr = scale dS^T Qr
+        dq = R_m^T dQr,  dk = R_n^T dKr  (the rotation is orthogonal)
+
+    ``q``, ``do`` [Sq, d]; ``k``, ``v`` [Skv, d]; positions as in
+    :func:`attention_rows`.  Returns (dq, dk, dv) in float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    q_pos = np.asarray(q_pos)
+    k_pos = np.asarray(k_pos)
+    qr = _rope.rotate(q, q_pos, theta)
+    kr = _rope.rotate(k, k_pos, theta)
+    logits = scale * (qr @ kr.T)
+    vis = visible(q_pos[:, None], k_pos[None, :], mask, sink, window)
+    logits = np.where(vis, logits, -np.inf)
+    mx = logits.max(axis=1, keepdims=True)
+    mx = np.where(np.isfinite(mx), mx, 0.0)
+    p = np.exp(logits - mx)
+    tot = p.sum(axis=1, keepdims=True)
+    p = np.where(tot > 0, p / np.where(tot > 0, tot, 1.0), 0.0)
+    dv = p.T @ do
+    dp = do @ v.T
+    D = (p * dp).sum(axis=1, keepdims=True)
+    ds = p * (dp - D)
+    dqr = scale * (ds @ kr)
+    dkr = scale * (ds.T @ qr)
+    # R^T is the rotation by the negated angle
+    dq = _rope.rotate(dqr, q_pos, -np.asarray(theta))
+    dk = _rope.rotate(dkr, k_pos, -np.asarray(theta))
+    return dq, dk, dv

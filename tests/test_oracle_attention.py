@@ -291,3 +291,48 @@ def test_merge_partials_ignores_the_output_of_an_empty_partial():
     o, lse = A.merge_partials([(o_a, np.array([-np.inf, -np.inf])), (np.ones((2, 3)), np.array([0.5, -np.inf]))])
     assert np.all(o[0] == 1.0) and lse[0] == 0.5
     assert np.all(o[1] == 0.0) and np.isneginf(lse[1])
+
+
+@pytest.mark.parametrize("mask,sink,window", [("causal", 0, 0), ("sink_window", 1, 3), ("none", 0, 0)])
+def test_backward_matches_finite_differences(mask, sink, window):
+    """The hand-derived backward against central differences of the forward
+    oracle's loss L = sum(O * G): independent of the chain-rule algebra."""
+    rng = np.random.default_rng(31)
+    S, d = 7, 6
+    q, k, v, g = rng.standard_normal((4, S, d))
+    theta = rope.base_frequencies(d, 100.0) / 3.0
+    pos = np.arange(S)
+    scale = 0.6
+
+    def loss(q_, k_, v_):
+        qr = rope.rotate(q_, pos, theta)
+        kr = rope.rotate(k_, pos, theta)
+        o, _ = A.attention_rows(qr, pos, kr, v_, mask, sink, window, scale)
+        return float((o * g).sum())
+
+    dq, dk, dv = A.backward_head(q, k, v, g, pos, pos, theta, scale, mask, sink, window)
+    h = 1e-6
+    for arr, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            dn = loss(*args)
+            num[idx] = (up - dn) / (2 * h)
+        np.testing.assert_allclose(grad, num, atol=1e-7, rtol=1e-6)
+
+
+def test_backward_rows_and_blocks_are_consistent():
+    """dV summed over query blocks equals dV of the whole (gradients are sums
+    over query rows), and D = rowsum(dO * O)."""
+    rng = np.random.default_rng(32)
+    S, d = 12, 4
+    q, k, v, g = rng.standard_normal((4, S, d))
+    theta = rope.base_frequencies(d, 1e4)
+    pos = np.arange(S)
+    _, _, dv = A.backward_head(q, k, v, g, pos, pos, theta, 0.5, "causal")
+    _, _, dv_a = A.backward_head(q[:5], k, v, g[:5], pos[:5], pos, theta, 0.5, "causal")
+    _, _, dv_b = A.backward_head(q[5:], k, v, g[5:], pos[5:], pos, theta, 0.5, "causal")
+    np.testing.assert_allclose(dv, dv_a + dv_b, atol=1e-12)

@@ -102,6 +102,10 @@ def load_library():
                                             I32, I32, _i64x3, _i64x3, _i64x3, _i64x3, I32, I32, I32,
                                             ctypes.c_float, _P, SZ, _P]),
         "attn_merge_partial": (I32, [_P, _P, _P, _P, _P, I32, I32, I32, I32, I32, _i64x3, _i64x3, _i64x3, _P]),
+        "yr_bwd_workspace_bytes": (SZ, [cfgp, I32, I32, I32, I32, I32, I32]),
+        "attn_bwd": (I32, [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32, I32, I32,
+                           _i64x3, _i64x3, _i64x3, _i64x3, _i64x3, _i64x3, _i64x3, _i64x3, I32, I32, I32,
+                           ctypes.c_float, _P, SZ, _P]),
         "yr_decode_auto_splits": (I32, [I32, I32, I32, I32]),
         "yr_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
         "attn_fwd_decode_sinkwindow": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32, I32,
@@ -260,6 +264,38 @@ def attn_merge_partial(o_acc, lse_acc, o_part, lse_part, out=None, stream=None):
                                   _strides(o_part), _strides(out) if out is not None else _i64x3(0, 0, 0),
                                   _stream(stream)))
     return o_acc, lse_acc
+
+
+def attn_bwd(cfg: RopeConfig, q, k, v, o, dout, lse, mask: str = "causal", sink: int = 0, window: int = 0,
+             softmax_scale: float = 0.0, out_dtype: torch.dtype | None = None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd_prefill with respect to the
+    unrotated q [B, Hq, S, d], k, v [B, Hkv, S, d], given o, dout and the
+    forward's lse [B, Hq, S]."""
+    lib = load_library()
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, S, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shapes: q, o, dout [B, Hq, S, d]; k, v [B, Hkv, S, d]")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise ValueError("q, k, v, o and dout must share a dtype")
+    if lse.dtype != torch.float32 or lse.shape != (B, Hq, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, Hq, S]")
+    od = q.dtype if out_dtype is None else out_dtype
+    dq = torch.empty(B, Hq, S, d, dtype=od, device=q.device)
+    dk = torch.empty(B, Hkv, S, d, dtype=od, device=q.device)
+    dv = torch.empty(B, Hkv, S, d, dtype=od, device=q.device)
+    c = cfg.c()
+    code = _dtype_code(q)
+    need = int(lib.yr_bwd_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, S, d))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.attn_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), code, _dtype_code(dq), B, Hq, Hkv, S, d, _strides(q), _strides(k),
+                        _strides(v), _strides(o), _strides(dout), _strides(dq), _strides(dk), _strides(dv),
+                        MASK[mask], int(sink), int(window), float(softmax_scale), _ptr(workspace),
+                        0 if workspace is None else workspace.numel() * workspace.element_size(),
+                        _stream(stream)))
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits=0) -> int:

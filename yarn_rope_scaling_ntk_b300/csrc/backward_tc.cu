@@ -1,0 +1,635 @@
+// attn_bwd: gradients of the exact softmax attention with the rotation applied
+// to Q and K, on the tcgen05 tensor cores of sm_103a.
+//
+// For O = softmax(scale * Qr Kr^T) V (Qr, Kr the rotated q and k; "Context
+// Window Scaling ...", Section 1 for the attention and Section 2 for the
+// rotation), with dO the gradient of the output, LSE the forward's row
+// log-sum-exp and D = rowsum(dO * O):
+//   P = exp(scale S - LSE),  dP = dO V^T,  dS = P * (dP - D)
+//   dV = P^T dO,  dKr = scale dS^T Qr,  dQr = scale dS Kr
+//   dk = R_n^T dKr,  dq = R_m^T dQr  (the rotation is orthogonal).
+// Two kernels, each one CTA per 128-row tile, 192 threads:
+//   bwd_kv_kernel: a 128-key tile of one (batch, KV head) walks the query
+//     tiles (of every query head of its group) that see it.  TMEM: S^T | dP^T
+//     | dV | dK; P^T and dS^T are written as bf16 over the first 64 columns of
+//     S^T and dP^T and feed the dV and dK products from TMEM.
+//   bwd_q_kernel: a 128-query tile walks its key tiles.  TMEM: S | dP | dQ;
+//     dS overwrites S and feeds the dQ product.
+// Roles: warps 0-3 one tile row per thread (TMEM lane), warp 4 MMA (converged,
+// one elected lane issues), warp 5 TMA producer.  The epilogues apply the
+// softmax scale and the inverse rotation.  Every wait is bounded.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace yr {
+namespace {
+
+using namespace tc;
+
+constexpr int BT = 128;        // rows per tile
+constexpr int kThreads = 192;  // warps 0-3 rows, 4 MMA, 5 TMA
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr int NS = 2;          // pipeline stages
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  int B, Hq, Hkv, S, group, n_tiles;
+  int mask, sink, window;
+  float scale_log2;  // scale * log2(e)
+  float scale;       // softmax scale (applied to dQ and dK)
+  const float* lse;  // [B, Hq, S], natural log
+  const float* dsum; // [B, Hq, S], rowsum(dO * O)
+  void* out_a;       // dK (kv kernel) or dQ (q kernel)
+  int64_t oas[3];
+  void* out_b;       // dV (kv kernel)
+  int64_t obs[3];
+  int out_bf16;
+  int* status;
+  RopeFreqs f;       // frequencies of the inverse rotation
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool visible(const BwdParams& p, int m, int n) {
+  if (p.mask == YR_MASK_NONE) return true;
+  if (n > m) return false;
+  return p.mask != YR_MASK_SINK_WINDOW || n < p.sink || m - n < p.window;
+}
+
+// Does a (query tile, key tile) pair need the element mask?
+__device__ __forceinline__ bool tile_needs_mask(const BwdParams& p, int m0, int n0) {
+  if (p.mask == YR_MASK_NONE) return false;
+  const int m1 = m0 + BT - 1, n1 = n0 + BT - 1;
+  if (n1 > m0) return true;  // some key is after some query
+  // some non-sink key farther than the window from some query
+  return p.mask == YR_MASK_SINK_WINDOW && n1 >= p.sink && m1 - max(n0, p.sink) >= p.window;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Query tiles that see key tile kt: [lo, hi] (hi < lo when none).
+__device__ __forceinline__ void query_tiles(const BwdParams& p, int kt, int& lo, int& hi) {
+  lo = p.mask == YR_MASK_NONE ? 0 : kt;
+  hi = p.n_tiles - 1;
+  const int n0 = kt * BT, n1 = n0 + BT - 1;
+  if (p.mask == YR_MASK_SINK_WINDOW && n0 >= p.sink) hi = min(hi, (n1 + p.window - 1) / BT);
+}
+
+// Key tiles that query tile qt sees: sink tiles [0, sink_hi] and the window
+// tiles [w_lo, hi]; returns the key tile of step u, or -1 past the end.
+struct KeyWalk {
+  int hi, sink_hi, w_lo;
+  __device__ void init(const BwdParams& p, int qt) {
+    const int m0 = qt * BT, m1 = m0 + BT - 1;
+    hi = p.mask == YR_MASK_NONE ? p.n_tiles - 1 : qt;
+    sink_hi = -1;
+    w_lo = 0;
+    if (p.mask == YR_MASK_SINK_WINDOW) {
+      sink_hi = p.sink > 0 ? min(hi, (p.sink - 1) / BT) : -1;
+      const int first = m0 - p.window + 1;  // the first key row m0 sees
+      w_lo = first <= 0 ? 0 : first / BT;
+      if (w_lo <= sink_hi + 1) { w_lo = 0; sink_hi = -1; }
+    }
+    (void)m1;
+  }
+  __device__ int count() const { return (sink_hi + 1) + (hi - w_lo + 1); }
+  __device__ int tile(int u) const { return u <= sink_hi ? u : w_lo + (u - sink_hi - 1); }
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kTile = BT * D * 2;  // bytes of a 128-row bf16 tile
+  static constexpr int kVec = BT * 4;       // 128 floats
+  // kv kernel: K, V once; per stage Q, dO, LSE, D
+  static constexpr int kvK = 0, kvV = kTile, kvStage0 = 2 * kTile;
+  static constexpr int kvStage = 2 * kTile + 2 * 1024;  // Q | dO | LSE | D (vectors padded to 1 KB)
+  static constexpr int kvBytes = kvStage0 + NS * kvStage;
+  // q kernel: Q, dO once; per stage K, V
+  static constexpr int qQ = 0, qDO = kTile, qStage0 = 2 * kTile;
+  static constexpr int qStage = 2 * kTile;
+  static constexpr int qBytes = qStage0 + NS * qStage;
+};
+
+// Row `row` of a 128 x D fp32 TMEM block -> global, scaled by `mult` and,
+// when `unrotate`, rotated back by -row * theta (pairs (i, i + D/2)).
+// Columns [32c, 32c + 32) and their partners [D/2 + 32c, ...) are handled
+// together, 64 values at a time.
+template <int D>
+__device__ __forceinline__ void store_rows(const BwdParams& p, uint32_t taddr, void* out, const int64_t st[3],
+                                           int b, int h, int row, float mult, bool unrotate, bool have) {
+  char* dst = static_cast<char*>(out) + (b * st[0] + h * st[1] + (int64_t)row * st[2]) * (p.out_bf16 ? 2 : 4);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t lo[32], hi[32];
+    if (have) {
+      tmem_ld32(taddr + c * 32, lo);
+      tmem_ld32(taddr + D / 2 + c * 32, hi);
+      tmem_ld_wait();
+      reg_fence32(lo);
+      reg_fence32(hi);
+    }
+    float a[32], bb[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      a[e] = have ? __uint_as_float(lo[e]) * mult : 0.f;
+      bb[e] = have ? __uint_as_float(hi[e]) * mult : 0.f;
+    }
+    if (unrotate && !p.f.identity) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float cs, sn;
+        turn_cos_sin<true>((float)row, p.f.f[c * 32 + e], cs, sn);
+        const float x = a[e], y = bb[e];
+        a[e] = x * cs + y * sn;
+        bb[e] = y * cs - x * sn;
+      }
+    }
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const float* v = part ? bb : a;
+      const int col = part * (D / 2) + c * 32;
+      if (p.out_bf16) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + col * 2);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                             pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+      } else {
+        float4* d4 = reinterpret_cast<float4*>(dst + col * 4);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per (key tile, batch, KV head); key tiles ascending (the
+// causal tiles with the most query tiles first).
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const __grid_constant__ BwdParams p) {
+  using C = Cfg<D>;
+  constexpr int ATOMS = D / 64;
+  constexpr int ATOM_BYTES = BT * 128;
+  constexpr uint32_t ID_SS = idesc_bf16_f32(BT, BT, false);  // [128 x D] x [128 x D]^T
+  constexpr uint32_t ID_TS = idesc_bf16_f32(BT, D, true);    // TMEM [128 x 128] x smem [128 x D]
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t kv_full, full[NS], empty[NS], s_full, p_full, o_done, drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.Hkv;
+  const int kt = (int)(blockIdx.x / BH);
+  const int bkv = blockIdx.x % BH;
+  const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
+  const int n0 = kt * BT;
+  int qlo, qhi;
+  query_tiles(p, kt, qlo, qhi);
+  const int per_head = max(0, qhi - qlo + 1);
+  const int iters = per_head * p.group;  // (query head of the group, query tile)
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&kv_full, 1);
+    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(&s_full, 1);
+    mbar_init(&p_full, 4);
+    mbar_init(&o_done, 1);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
+      // with no query tile to visit nothing is loaded (nobody would wait)
+      if (iters > 0) {
+        mbar_arrive_expect_tx(&kv_full, 2 * C::kTile);
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_load_4d(smem + C::kvK + a * ATOM_BYTES, &tk, &kv_full, a * 64, n0, hkv, b);
+          tma_load_4d(smem + C::kvV + a * ATOM_BYTES, &tv, &kv_full, a * 64, n0, hkv, b);
+        }
+      }
+      int uses[NS] = {0, 0};
+      for (int i = 0; i < iters; ++i) {
+        const int s = i % NS;
+        const int hq = hkv * p.group + i / per_head;
+        const int m0 = (qlo + i % per_head) * BT;
+        if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, &abort_flag, p.status, 51)) break;
+        uint8_t* st = smem + C::kvStage0 + s * C::kvStage;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kTile + 2 * C::kVec);
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_load_4d(st + a * ATOM_BYTES, &tq, &full[s], a * 64, m0, hq, b);
+          tma_load_4d(st + C::kTile + a * ATOM_BYTES, &tdo, &full[s], a * 64, m0, hq, b);
+        }
+        const int64_t row0 = ((int64_t)b * p.Hq + hq) * p.S + m0;
+        bulk_g2s(st + 2 * C::kTile, p.lse + row0, C::kVec, &full[s]);
+        bulk_g2s(st + 2 * C::kTile + 1024, p.dsum + row0, C::kVec, &full[s]);
+        ++uses[s];
+      }
+      if (abort_flag) {
+        if (iters > 0) mbar_wait_drain(&kv_full, 0, 200000000ll);
+        for (int s = 0; s < NS; ++s)
+          if (uses[s]) mbar_wait_drain(&full[s], (uses[s] - 1) & 1, 200000000ll);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    const bool leader = elect_one();
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + C::kvK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kvV), 16, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
+    };
+    bool ok = iters == 0 || wait(&kv_full, 0, 61);
+    for (int i = 0; ok && i < iters; ++i) {
+      const int s = i % NS;
+      const uint32_t st = smem_u32(smem + C::kvStage0 + s * C::kvStage);
+      if (!wait(&full[s], (i / NS) & 1, 62)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dQk = sdesc_sw128(st, 16, 1024), dDOk = sdesc_sw128(st + C::kTile, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + C_S, dK + off, dQk + off, ID_SS, kk > 0);      // S^T = K Q^T
+          mma_ss(tmem + C_DP, dV + off, dDOk + off, ID_SS, kk > 0);    // dP^T = V dO^T
+        }
+        mma_commit(&s_full);
+      }
+      __syncwarp();
+      if (!wait(&p_full, i & 1, 63)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dQn = sdesc_sw128(st, ATOM_BYTES, 1024), dDOn = sdesc_sw128(st + C::kTile, ATOM_BYTES, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk) {
+          const uint64_t off = (uint64_t)(kk * 2048 >> 4);
+          mma_ts(tmem + C_DV, tmem + C_S + kk * 8, dDOn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dO
+          mma_ts(tmem + C_DK, tmem + C_DP + kk * 8, dQn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T Q
+        }
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(&o_done);
+      mma_commit(&drain);
+      mbar_wait_drain(&drain, 0, 200000000ll);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- rows: warps 0-3, thread r = key row n0 + r ----------
+    const int r = warp * 32 + lane;
+    const int n = n0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    bool ok = true;
+    for (int i = 0; i < iters; ++i) {
+      const int s = i % NS;
+      const int m0 = (qlo + i % per_head) * BT;
+      const float* sL = reinterpret_cast<const float*>(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);
+      const float* sD = sL + 256;  // the D vector sits 1 KB after LSE
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full, i & 1, &abort_flag, p.status, 71));
+      // the LSE / D vectors of this stage landed with full[s] (already
+      // complete: the MMA waited for it before the products of s_full); the
+      // stage is refilled only after this group's p_full below
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / NS) & 1, &abort_flag, p.status, 73));
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = tile_needs_mask(p, m0, n0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // query columns 64h .. 64h + 63
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(lane_addr + C_S + h * 64, sr[0]);
+        tmem_ld32(lane_addr + C_S + h * 64 + 32, sr[1]);
+        tmem_ld32(lane_addr + C_DP + h * 64, dr[0]);
+        tmem_ld32(lane_addr + C_DP + h * 64 + 32, dr[1]);
+        tmem_ld_wait();
+        reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+        uint32_t pk[32], dk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int c = h * 64 + 2 * e + t;
+            const float sv = __uint_as_float(sr[(2 * e + t) >> 5][(2 * e + t) & 31]);
+            const float dv = __uint_as_float(dr[(2 * e + t) >> 5][(2 * e + t) & 31]);
+            float pr = ex2(fmaf(sv, p.scale_log2, -sL[c] * kLog2e));
+            if (need_mask && !visible(p, m0 + c, n)) pr = 0.f;
+            pp[t] = pr;
+            dd[t] = pr * (dv - sD[c]);
+          }
+          pk[e] = pack_bf16(pp[0], pp[1]);
+          dk[e] = pack_bf16(dd[0], dd[1]);
+        }
+        tmem_st32(lane_addr + C_S + h * 32, pk);
+        tmem_st32(lane_addr + C_DP + h * 32, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full);
+    }
+    if (__all_sync(0xffffffffu, ok && !abort_flag)) {
+      bool have = iters > 0;
+      if (have) have = __all_sync(0xffffffffu, mbar_wait(&o_done, 0, &abort_flag, p.status, 72));
+      tc_fence_after();
+      if (!abort_flag) {
+        store_rows<D>(p, lane_addr + C_DV, p.out_b, p.obs, b, hkv, n, 1.f, false, have);
+        store_rows<D>(p, lane_addr + C_DK, p.out_a, p.oas, b, hkv, n, p.scale, true, have);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (query tile, batch, query head); heaviest query tiles first.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                 const __grid_constant__ BwdParams p) {
+  using C = Cfg<D>;
+  constexpr int ATOMS = D / 64;
+  constexpr int ATOM_BYTES = BT * 128;
+  constexpr uint32_t ID_SS = idesc_bf16_f32(BT, BT, false);
+  constexpr uint32_t ID_TS = idesc_bf16_f32(BT, D, true);
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t q_full, full[NS], empty[NS], s_full, p_full, o_done, drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.Hq;
+  const int qt = p.n_tiles - 1 - (int)(blockIdx.x / BH);
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.Hq, hq = bh % p.Hq;
+  const int hkv = hq / p.group;
+  const int m0 = qt * BT;
+  KeyWalk walk;
+  walk.init(p, qt);
+  const int iters = walk.count();
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&q_full, 1);
+    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(&s_full, 1);
+    mbar_init(&p_full, 4);
+    mbar_init(&o_done, 1);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
+      if (iters > 0) {
+        mbar_arrive_expect_tx(&q_full, 2 * C::kTile);
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_load_4d(smem + C::qQ + a * ATOM_BYTES, &tq, &q_full, a * 64, m0, hq, b);
+          tma_load_4d(smem + C::qDO + a * ATOM_BYTES, &tdo, &q_full, a * 64, m0, hq, b);
+        }
+      }
+      int uses[NS] = {0, 0};
+      for (int i = 0; i < iters; ++i) {
+        const int s = i % NS;
+        const int nk0 = walk.tile(i) * BT;
+        if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, &abort_flag, p.status, 81)) break;
+        uint8_t* st = smem + C::qStage0 + s * C::qStage;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kTile);
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_load_4d(st + a * ATOM_BYTES, &tk, &full[s], a * 64, nk0, hkv, b);
+          tma_load_4d(st + C::kTile + a * ATOM_BYTES, &tv, &full[s], a * 64, nk0, hkv, b);
+        }
+        ++uses[s];
+      }
+      if (abort_flag) {
+        if (iters > 0) mbar_wait_drain(&q_full, 0, 200000000ll);
+        for (int s = 0; s < NS; ++s)
+          if (uses[s]) mbar_wait_drain(&full[s], (uses[s] - 1) & 1, 200000000ll);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    const bool leader = elect_one();
+    const uint64_t dQk = sdesc_sw128(smem_u32(smem + C::qQ), 16, 1024);
+    const uint64_t dDOk = sdesc_sw128(smem_u32(smem + C::qDO), 16, 1024);
+    auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
+    };
+    bool ok = iters == 0 || wait(&q_full, 0, 91);
+    for (int i = 0; ok && i < iters; ++i) {
+      const int s = i % NS;
+      const uint32_t st = smem_u32(smem + C::qStage0 + s * C::qStage);
+      if (!wait(&full[s], (i / NS) & 1, 92)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dKk = sdesc_sw128(st, 16, 1024), dVk = sdesc_sw128(st + C::kTile, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + C_S, dQk + off, dKk + off, ID_SS, kk > 0);     // S = Q K^T
+          mma_ss(tmem + C_DP, dDOk + off, dVk + off, ID_SS, kk > 0);   // dP = dO V^T
+        }
+        mma_commit(&s_full);
+      }
+      __syncwarp();
+      if (!wait(&p_full, i & 1, 93)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t dKn = sdesc_sw128(st, ATOM_BYTES, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          mma_ts(tmem + C_DQ, tmem + C_S + kk * 8, dKn + (uint64_t)(kk * 2048 >> 4), ID_TS,
+                 (i > 0 || kk > 0) ? 1u : 0u);  // dQ += dS K
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(&o_done);
+      mma_commit(&drain);
+      mbar_wait_drain(&drain, 0, 200000000ll);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- rows: warps 0-3, thread r = query row m0 + r --------
+    const int r = warp * 32 + lane;
+    const int m = m0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int64_t row = ((int64_t)b * p.Hq + hq) * p.S + m;
+    const float lse_l2 = p.lse[row] * kLog2e;
+    const float dsum = p.dsum[row];
+    bool ok = true;
+    for (int i = 0; i < iters; ++i) {
+      const int nk0 = walk.tile(i) * BT;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full, i & 1, &abort_flag, p.status, 101));
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = tile_needs_mask(p, m0, nk0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // key columns 64h .. 64h + 63
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(lane_addr + C_S + h * 64, sr[0]);
+        tmem_ld32(lane_addr + C_S + h * 64 + 32, sr[1]);
+        tmem_ld32(lane_addr + C_DP + h * 64, dr[0]);
+        tmem_ld32(lane_addr + C_DP + h * 64 + 32, dr[1]);
+        tmem_ld_wait();
+        reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+        uint32_t dk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float dd[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int c = h * 64 + 2 * e + t;
+            const float sv = __uint_as_float(sr[(2 * e + t) >> 5][(2 * e + t) & 31]);
+            const float dv = __uint_as_float(dr[(2 * e + t) >> 5][(2 * e + t) & 31]);
+            float pr = ex2(fmaf(sv, p.scale_log2, -lse_l2));
+            if (need_mask && !visible(p, m, nk0 + c)) pr = 0.f;
+            dd[t] = pr * (dv - dsum);
+          }
+          dk[e] = pack_bf16(dd[0], dd[1]);
+        }
+        tmem_st32(lane_addr + C_S + h * 32, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full);
+    }
+    if (__all_sync(0xffffffffu, ok && !abort_flag)) {
+      bool have = iters > 0;
+      if (have) have = __all_sync(0xffffffffu, mbar_wait(&o_done, 0, &abort_flag, p.status, 102));
+      tc_fence_after();
+      if (!abort_flag) store_rows<D>(p, lane_addr + C_DQ, p.out_a, p.oas, b, hq, m, p.scale, true, have);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// D = rowsum(dO * O): one warp per row of [B, H, S, d].
+template <typename T>
+__global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, float* dsum, int B, int H, int S, int d,
+                                                   int64_t ds0, int64_t ds1, int64_t ds2, int64_t os0, int64_t os1,
+                                                   int64_t os2) {
+  const int64_t rows = (int64_t)B * H * S;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int s = (int)(row % S);
+  const int64_t bh = row / S;
+  const int h = (int)(bh % H), b = (int)(bh / H);
+  const T* dr = dout + b * ds0 + h * ds1 + (int64_t)s * ds2;
+  const T* orow = o + b * os0 + h * os1 + (int64_t)s * os2;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) acc = fmaf(static_cast<float>(dr[c]), static_cast<float>(orow[c]), acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) dsum[row] = acc;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, a.q, a.B, a.Hq, a.S, D, a.qs) || !make_map(&mk, a.k, a.B, a.Hkv, a.S, D, a.ks) ||
+      !make_map(&mv, a.v, a.B, a.Hkv, a.S, D, a.vs) || !make_map(&mdo, a.dout, a.B, a.Hq, a.S, D, a.dos))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.S = a.S; p.group = a.Hq / a.Hkv; p.n_tiles = a.S / BT;
+  p.mask = a.mask; p.sink = a.sink; p.window = a.window;
+  p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;
+  p.lse = a.lse; p.dsum = a.dsum;
+  p.out_bf16 = a.out_bf16;
+  p.f = a.f;
+  p.status = device_status_word();
+  if (!p.status) return cudaErrorInvalidValue;
+  using C = Cfg<D>;
+  // dK, dV
+  p.out_a = a.dk; p.out_b = a.dv;
+  for (int i = 0; i < 3; ++i) { p.oas[i] = a.dks[i]; p.obs[i] = a.dvs[i]; }
+  int smem = C::kvBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_kv_kernel<D><<<(unsigned)(p.n_tiles * a.B * a.Hkv), kThreads, smem, st>>>(mq, mk, mv, mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dQ
+  p.out_a = a.dq; p.out_b = nullptr;
+  for (int i = 0; i < 3; ++i) p.oas[i] = a.dqs[i];
+  smem = C::qBytes + 1024;
+  e = cudaFuncSetAttribute(bwd_q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bwd_q_kernel<D><<<(unsigned)(p.n_tiles * a.B * a.Hq), kThreads, smem, st>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, int B, int H, int S, int d,
+                        const int64_t ds[3], const int64_t os[3], cudaStream_t st) {
+  const int64_t rows = (int64_t)B * H * S;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (bf16)
+    dsum_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(o), dsum, B, H, S, d, ds[0], ds[1],
+        ds[2], os[0], os[1], os[2]);
+  else
+    dsum_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float*>(dout), static_cast<const float*>(o),
+                                                         dsum, B, H, S, d, ds[0], ds[1], ds[2], os[0], os[1], os[2]);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {
+  if (a.S % BT != 0) return cudaErrorInvalidValue;
+  return a.d == 128 ? launch_bwd_d<128>(a, st) : launch_bwd_d<64>(a, st);
+}
+
+}  // namespace yr

@@ -361,6 +361,107 @@ yr_status attn_merge_partial(float* o_acc, float* lse_acc, const float* o_part, 
   return e == cudaSuccess ? YR_OK : cuda_fail(e, "attn_merge_partial launch");
 }
 
+static size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+size_t yr_bwd_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t S, int32_t d) {
+  if (!cfg || B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || d <= 0) return 0;
+  const size_t q = (size_t)B * Hq * S * d * 2, kv = (size_t)B * Hkv * S * d * 2;
+  size_t bytes = align16(q) + align16(kv);                   // rotated Q, K
+  if (in_dtype == YR_F32) bytes += align16(kv) + align16(q);  // bf16 V, dO
+  bytes += align16((size_t)B * Hq * S * 4);                  // D = rowsum(dO * O)
+  return bytes;
+}
+
+yr_status attn_bwd(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v, const void* o,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int32_t in_dtype,
+                   int32_t out_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
+                   const int64_t q_strides[3], const int64_t k_strides[3], const int64_t v_strides[3],
+                   const int64_t o_strides[3], const int64_t do_strides[3], const int64_t dq_strides[3],
+                   const int64_t dk_strides[3], const int64_t dv_strides[3], int32_t mask, int32_t sink,
+                   int32_t window, float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (!cfg) return fail(YR_ERR_INVALID_ARG, "attn_bwd: cfg is NULL");
+  if (in_dtype != YR_F32 && in_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "attn_bwd: dtype %d", in_dtype);
+  if (out_dtype != YR_F32 && out_dtype != YR_BF16) return fail(YR_ERR_INVALID_ARG, "attn_bwd: out dtype %d", out_dtype);
+  if (B < 0 || Hq < 0 || Hkv < 0 || S < 0) return fail(YR_ERR_INVALID_ARG, "attn_bwd: negative shape");
+  if (d != 64 && d != 128) return fail(YR_ERR_UNSUPPORTED, "attn_bwd: head dimension %d (64 or 128)", d);
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return fail(YR_ERR_INVALID_ARG, "attn_bwd: Hq %% Hkv != 0");
+  if (S % 128 != 0) return fail(YR_ERR_UNSUPPORTED, "attn_bwd: S=%d must be a multiple of 128", S);
+  if (S > (1 << 24)) return fail(YR_ERR_INVALID_ARG, "attn_bwd: S above 2^24");
+  if (mask < YR_MASK_CAUSAL || mask > YR_MASK_NONE) return fail(YR_ERR_INVALID_ARG, "attn_bwd: mask %d", mask);
+  if (mask == YR_MASK_SINK_WINDOW && (sink < 0 || window < 1))
+    return fail(YR_ERR_INVALID_ARG, "attn_bwd: sink must be >= 0 and window >= 1");
+  const int64_t* strides[8] = {q_strides, k_strides, v_strides, o_strides, do_strides, dq_strides, dk_strides,
+                               dv_strides};
+  for (auto st : strides)
+    if (!st) return fail(YR_ERR_INVALID_ARG, "attn_bwd: strides are NULL");
+  RopeFreqs f;
+  yr_status st = build_rope_freqs(cfg, d, &f);
+  if (st != YR_OK) return st;
+  if (B == 0 || S == 0) return YR_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+    return fail(YR_ERR_INVALID_ARG, "attn_bwd: a required pointer is NULL");
+  const int elem = in_dtype == YR_BF16 ? 2 : 4, oelem = out_dtype == YR_BF16 ? 2 : 4;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !rows_aligned(q_strides, elem) ||
+      !rows_aligned(k_strides, elem) || !rows_aligned(v_strides, elem) || !rows_aligned(o_strides, elem) ||
+      !rows_aligned(do_strides, elem) || !rows_aligned(dq_strides, oelem) || !rows_aligned(dk_strides, oelem) ||
+      !rows_aligned(dv_strides, oelem))
+    return fail(YR_ERR_INVALID_ARG, "attn_bwd: pointers and strides must be 16-byte aligned");
+  const size_t need = yr_bwd_workspace_bytes(cfg, in_dtype, B, Hq, Hkv, S, d);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(YR_ERR_INVALID_ARG, "attn_bwd: workspace of %zu aligned bytes needed", need);
+
+  const double ms = f.mscale;
+  const double scale = softmax_scale > 0.f ? (double)softmax_scale : ms * ms / sqrt((double)d);
+  cudaStream_t cs = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  size_t off = 0;
+  BwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  auto prep = [&](const void* src, const int64_t* src_s, int H, bool rotate, const void** dst,
+                  int64_t* dst_s) -> cudaError_t {
+    void* out = ws + off;
+    const int64_t hs = (int64_t)S * d;
+    off += align16((size_t)B * H * hs * 2);
+    RopeLaunch r;
+    memset(&r, 0, sizeof(r));
+    r.x = src; r.y = out; r.in_bf16 = in_dtype == YR_BF16; r.out_bf16 = 1;
+    r.B = B; r.H = H; r.S = S; r.d = d;
+    dst_s[0] = (int64_t)H * hs; dst_s[1] = hs; dst_s[2] = d;
+    for (int i = 0; i < 3; ++i) { r.xs[i] = src_s[i]; r.ys[i] = dst_s[i]; }
+    RopeFreqs ff = f;
+    if (!rotate) ff.identity = 1;
+    *dst = out;
+    return launch_rope(r, ff, cs);
+  };
+  cudaError_t e = prep(q, q_strides, Hq, true, &a.q, a.qs);
+  if (e == cudaSuccess) e = prep(k, k_strides, Hkv, true, &a.k, a.ks);
+  if (e == cudaSuccess) {
+    if (in_dtype == YR_F32) {
+      e = prep(v, v_strides, Hkv, false, &a.v, a.vs);
+      if (e == cudaSuccess) e = prep(dout, do_strides, Hq, false, &a.dout, a.dos);
+    } else {
+      a.v = v; a.dout = dout;
+      for (int i = 0; i < 3; ++i) { a.vs[i] = v_strides[i]; a.dos[i] = do_strides[i]; }
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd rotation pass");
+  float* dsum = reinterpret_cast<float*>(ws + off);
+  e = launch_dsum(dout, o, in_dtype == YR_BF16, dsum, B, Hq, S, d, do_strides, o_strides, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd rowsum(dO * O)");
+  a.lse = lse; a.dsum = dsum;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.out_bf16 = out_dtype == YR_BF16;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.S = S; a.d = d;
+  for (int i = 0; i < 3; ++i) { a.dqs[i] = dq_strides[i]; a.dks[i] = dk_strides[i]; a.dvs[i] = dv_strides[i]; }
+  a.mask = mask; a.sink = sink; a.window = window;
+  a.scale = (float)scale;
+  a.f = f;
+  e = launch_bwd(a, cs);
+  return e == cudaSuccess ? YR_OK : cuda_fail(e, "attn_bwd launch");
+}
+
 int32_t yr_decode_auto_splits(int32_t B, int32_t Hkv, int32_t sink, int32_t window) {
   // Enough CTAs to cover two waves of the 148 SMs, without slices under 512
   // cache entries.

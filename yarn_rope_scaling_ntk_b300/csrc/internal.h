@@ -1,6 +1,7 @@
 // Private declarations shared by the host entry points and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,12 @@ yr_status cuda_fail(cudaError_t e, const char* what);
 
 // Address of the device status word (per device), set by bounded waits.
 int* device_status_word();
+
+// Number of SMs of the current device.
+int sm_count();
+// TMA map of a [B, H, S, D] bfloat16 tensor (element strides b, h, s): 4-D,
+// 64 x 128 boxes, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* base, int B, int H, int S, int D, const int64_t st[3]);
 
 // ---- launches (kernel files) ----------------------------------------------
 struct RopeLaunch {
@@ -82,6 +89,29 @@ struct PrefillLaunch {
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t st);
+
+// Attention backward (attn_bwd): q, k rotated bf16 copies, v and dout bf16.
+struct BwdLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const float* lse;
+  const float* dsum;
+  void* dq;
+  void* dk;
+  void* dv;
+  int out_bf16;
+  int B, Hq, Hkv, S, d;
+  int64_t qs[3], ks[3], vs[3], dos[3], dqs[3], dks[3], dvs[3];
+  int mask, sink, window;
+  float scale;
+  RopeFreqs f;
+};
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
+// D = rowsum(dO * O) of [B, H, S, d] tensors (bf16 when bf16 != 0, else f32).
+cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, int B, int H, int S, int d,
+                        const int64_t ds[3], const int64_t os[3], cudaStream_t st);
 
 // Exact merge of an attention partial into an accumulator (attn_merge_partial).
 struct MergeLaunch {

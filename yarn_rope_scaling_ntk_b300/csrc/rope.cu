@@ -106,16 +106,6 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeLaunch a, RopeFreqs f) {
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_rope(const RopeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
