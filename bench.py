@@ -411,6 +411,28 @@ def run_ours(args):
     del o
     torch.cuda.empty_cache()
 
+    # ---- backward of the same prefill (whole call: rotation, rowsum, dK/dV, dQ)
+    bwd = None
+    if not args.no_backward:
+        qb, kb, vb = W.prefill_inputs(w, dev)
+        ob, lseb = api.attn_fwd_prefill(cfg, qb, kb, vb, mask=w.mask, return_lse=True)
+        g = torch.Generator(device=dev).manual_seed(77)
+        dob = torch.randn(qb.shape, generator=g, device=dev).to(qb.dtype)
+        bws = torch.empty(api.lib_bwd_workspace_bytes(cfg, qb.dtype, w.B, w.Hq, w.Hkv, w.S, w.d),
+                          dtype=torch.uint8, device=dev)
+        bcall = lambda: api.attn_bwd(cfg, qb, kb, vb, ob, dob, lseb, mask=w.mask, workspace=bws)
+        for _ in range(2):
+            bcall()
+        bwd_ms = statistics.median(timed(bcall, 5, stream))
+        api.sync_status()
+        # algorithmic: dV, dP, dQ, dK and one recompute of S, 2 d flops each per visible pair
+        bflops = 2.5 * prefill_flops(w)
+        bwd = {"workload": w.name, "ms": bwd_ms, "TFLOP/s": bflops / (bwd_ms * 1e-3) / 1e12,
+               "frac_of_burst": bflops / (bwd_ms * 1e-3) / 1e12 / tf_burst,
+               "flops": "10 d per visible pair (the kernels do 14 d: S and dP are recomputed in both)"}
+        del qb, kb, vb, ob, lseb, dob, bws
+        torch.cuda.empty_cache()
+
     # ---- the other prefill workloads (whole fused call, device time) -------
     others = []
     if not args.no_other_workloads:
@@ -449,6 +471,7 @@ def run_ours(args):
                        "speedup_vs_bf16_cache": dec_ms / dec8_ms,
                        "roofline": {"bound": "hbm", "achieved": dec8_gbs, "peak": hbm, "unit": "GB/s",
                                     "frac": dec8_gbs / hbm, "traffic": None}},
+        "backward": bwd,
         "other_prefill_workloads": others,
         "rope_apply": {"workload": "Q and K of " + w.name, "value": rope_gbs, "unit": "GB/s",
                        "ms": rope_ms,
@@ -473,7 +496,17 @@ def run_part(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n = max(1, args.warmup) + max(1, args.steps)
-    if args.part in ("prefill", "rope"):
+    if args.part == "backward":
+        w = W.LLAMA2_7B if not args.small else replace(W.LLAMA2_7B, S=4096, name="llama2_7b_shape_S4096")
+        cfg = cfg_of(w)
+        q, k, v = W.prefill_inputs(w, dev)
+        o, lse = api.attn_fwd_prefill(cfg, q, k, v, mask=w.mask, return_lse=True)
+        dout = torch.randn(q.shape, device=dev).to(q.dtype)
+        ws = torch.empty(api.lib_bwd_workspace_bytes(cfg, q.dtype, w.B, w.Hq, w.Hkv, w.S, w.d),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(n):
+            api.attn_bwd(cfg, q, k, v, o, dout, lse, mask=w.mask, workspace=ws)
+    elif args.part in ("prefill", "rope"):
         w = W.LLAMA2_7B if not args.small else replace(W.LLAMA2_7B, S=4096, name="llama2_7b_shape_S4096")
         cfg = cfg_of(w)
         q, k, v = W.prefill_inputs(w, dev)
@@ -502,9 +535,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the attention backward")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the ring 128K and GQA prefill workloads")
-    ap.add_argument("--part", choices=["prefill", "decode", "rope"], default=None,
+    ap.add_argument("--part", choices=["prefill", "decode", "rope", "backward"], default=None,
                     help="profile one kernel family alone (prints no bench line)")
     ap.add_argument("--small", action="store_true", help="with --part: smaller workload")
     args = ap.parse_args()

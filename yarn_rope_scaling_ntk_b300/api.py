@@ -266,6 +266,12 @@ def attn_merge_partial(o_acc, lse_acc, o_part, lse_part, out=None, stream=None):
     return o_acc, lse_acc
 
 
+def lib_bwd_workspace_bytes(cfg: RopeConfig, dtype: torch.dtype, B, Hq, Hkv, S, d) -> int:
+    c = cfg.c()
+    code = F32 if dtype == torch.float32 else BF16
+    return int(load_library().yr_bwd_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, S, d))
+
+
 def attn_bwd(cfg: RopeConfig, q, k, v, o, dout, lse, mask: str = "causal", sink: int = 0, window: int = 0,
              softmax_scale: float = 0.0, out_dtype: torch.dtype | None = None, workspace=None, stream=None):
     """Gradients (dq, dk, dv) of attn_fwd_prefill with respect to the

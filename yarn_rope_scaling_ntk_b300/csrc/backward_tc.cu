@@ -15,9 +15,14 @@
 //     S^T and dP^T and feed the dV and dK products from TMEM.
 //   bwd_q_kernel: a 128-query tile walks its key tiles.  TMEM: S | dP | dQ;
 //     dS overwrites S and feeds the dQ product.
-// Roles: warps 0-3 one tile row per thread (TMEM lane), warp 4 MMA (converged,
-// one elected lane issues), warp 5 TMA producer.  The epilogues apply the
-// softmax scale and the inverse rotation.  Every wait is bounded.
+// Roles (384 threads): warps 0-3 and 4-7 are two row groups on the same TMEM
+// lanes (thread r owns tile row r), group 0 taking columns 0-63 and group 1
+// columns 64-127 of each S / dP tile, so two warps per SM sub-partition hide
+// each other's latency; warp 8 MMA (converged, one elected lane issues),
+// warp 9 TMA producer, warps 10-11 only lend registers (setmaxnreg).  Each
+// group writes its bf16 P / dS over its own, already read, columns (group 0
+// at 0-31, group 1 at 64-95).  The epilogues apply the softmax scale and the
+// inverse rotation.  Every wait is bounded.
 #include <math.h>
 #include <string.h>
 
@@ -31,19 +36,23 @@ namespace {
 using namespace tc;
 
 constexpr int BT = 128;        // rows per tile
-constexpr int kThreads = 192;  // warps 0-3 rows, 4 MMA, 5 TMA
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
+constexpr int kThreads = 384;  // warps 0-7 rows, 8 MMA, 9 TMA, 10-11 idle
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kRegsRows = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168
+constexpr uint32_t kRegsControl = 72;
+static_assert(2 * 128 * kRegsRows + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr int NS = 2;          // pipeline stages
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPrefetch = 4;   // iterations whose tiles the producer prefetches into L2
 
 struct BwdParams {
   int B, Hq, Hkv, S, group, n_tiles;
   int mask, sink, window;
   float scale_log2;  // scale * log2(e)
   float scale;       // softmax scale (applied to dQ and dK)
-  const float* lse;  // [B, Hq, S], natural log
+  const float* lse2; // [B, Hq, S], LSE * log2(e)
   const float* dsum; // [B, Hq, S], rowsum(dO * O)
   void* out_a;       // dK (kv kernel) or dQ (q kernel)
   int64_t oas[3];
@@ -58,6 +67,12 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ bool visible(const BwdParams& p, int m, int n) {
@@ -132,10 +147,12 @@ struct Cfg {
 // together, 64 values at a time.
 template <int D>
 __device__ __forceinline__ void store_rows(const BwdParams& p, uint32_t taddr, void* out, const int64_t st[3],
-                                           int b, int h, int row, float mult, bool unrotate, bool have) {
+                                           int b, int h, int row, float mult, bool unrotate, bool have, int c_begin,
+                                           int c_end) {
   char* dst = static_cast<char*>(out) + (b * st[0] + h * st[1] + (int64_t)row * st[2]) * (p.out_bf16 ? 2 : 4);
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
+    if (c < c_begin || c >= c_end) continue;
     uint32_t lo[32], hi[32];
     if (have) {
       tmem_ld32(taddr + c * 32, lo);
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&kv_full, 1);
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(&s_full, 1);
-    mbar_init(&p_full, 4);
+    mbar_init(&p_full, 8);  // one arrival per row warp
     mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -227,7 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   reg_dealloc<kRegsControl>();
+   if (warp == kLoadWarp) {
     if (lane == 0) {
       tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
       // with no query tile to visit nothing is loaded (nobody would wait)
@@ -239,10 +258,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       int uses[NS] = {0, 0};
+      // the tiles of the first iterations go to L2 ahead of their loads
+      auto prefetch = [&](int i) {
+        if (i >= iters) return;
+        const int hq = hkv * p.group + i / per_head;
+        const int m0 = (qlo + i % per_head) * BT;
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_prefetch_l2_4d(&tq, a * 64, m0, hq, b);
+          tma_prefetch_l2_4d(&tdo, a * 64, m0, hq, b);
+        }
+        const int64_t row0 = ((int64_t)b * p.Hq + hq) * p.S + m0;
+        bulk_prefetch_l2(p.lse2 + row0, C::kVec);
+        bulk_prefetch_l2(p.dsum + row0, C::kVec);
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch(i);
       for (int i = 0; i < iters; ++i) {
         const int s = i % NS;
         const int hq = hkv * p.group + i / per_head;
         const int m0 = (qlo + i % per_head) * BT;
+        prefetch(i + kPrefetch);
         if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, &abort_flag, p.status, 51)) break;
         uint8_t* st = smem + C::kvStage0 + s * C::kvStage;
         mbar_arrive_expect_tx(&full[s], 2 * C::kTile + 2 * C::kVec);
@@ -251,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(st + C::kTile + a * ATOM_BYTES, &tdo, &full[s], a * 64, m0, hq, b);
         }
         const int64_t row0 = ((int64_t)b * p.Hq + hq) * p.S + m0;
-        bulk_g2s(st + 2 * C::kTile, p.lse + row0, C::kVec, &full[s]);
+        bulk_g2s(st + 2 * C::kTile, p.lse2 + row0, C::kVec, &full[s]);
         bulk_g2s(st + 2 * C::kTile + 1024, p.dsum + row0, C::kVec, &full[s]);
         ++uses[s];
       }
@@ -262,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
     const uint64_t dK = sdesc_sw128(smem_u32(smem + C::kvK), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kvV), 16, 1024);
@@ -293,8 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk) {
           const uint64_t off = (uint64_t)(kk * 2048 >> 4);
-          mma_ts(tmem + C_DV, tmem + C_S + kk * 8, dDOn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dO
-          mma_ts(tmem + C_DK, tmem + C_DP + kk * 8, dQn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T Q
+          const uint32_t a_off = (kk >> 2) * 64 + (kk & 3) * 8;  // group (kk / 4)'s packed columns
+          mma_ts(tmem + C_DV, tmem + C_S + a_off, dDOn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dO
+          mma_ts(tmem + C_DK, tmem + C_DP + a_off, dQn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T Q
         }
         mma_commit(&empty[s]);
       }
@@ -306,54 +341,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&drain, 0, 200000000ll);
     }
     __syncwarp();
+   }
   } else {
-    // ---------------- rows: warps 0-3, thread r = key row n0 + r ----------
-    const int r = warp * 32 + lane;
+    reg_alloc<kRegsRows>();
+    // ---------------- rows: thread r = key row n0 + r; group wg takes the
+    // query columns 64 wg .. 64 wg + 63 of each S^T / dP^T tile ---------------
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int n = n0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int col0 = wg * 64;
+    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < iters; ++i) {
       const int s = i % NS;
       const int m0 = (qlo + i % per_head) * BT;
-      const float* sL = reinterpret_cast<const float*>(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);
-      const float* sD = sL + 256;  // the D vector sits 1 KB after LSE
+      const uint32_t vec = smem_u32(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);  // LSE*log2e | D
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full, i & 1, &abort_flag, p.status, 71));
       // the LSE / D vectors of this stage landed with full[s] (already
       // complete: the MMA waited for it before the products of s_full); the
-      // stage is refilled only after this group's p_full below
+      // stage is refilled only after both groups' p_full below
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / NS) & 1, &abort_flag, p.status, 73));
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = tile_needs_mask(p, m0, n0);
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(lane_addr + C_S + col0, sr[0]);
+      tmem_ld32(lane_addr + C_S + col0 + 32, sr[1]);
+      tmem_ld32(lane_addr + C_DP + col0, dr[0]);
+      tmem_ld32(lane_addr + C_DP + col0 + 32, dr[1]);
+      tmem_ld_wait();
+      reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+      uint32_t pk[32], dk[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // query columns 64h .. 64h + 63
-        uint32_t sr[2][32], dr[2][32];
-        tmem_ld32(lane_addr + C_S + h * 64, sr[0]);
-        tmem_ld32(lane_addr + C_S + h * 64 + 32, sr[1]);
-        tmem_ld32(lane_addr + C_DP + h * 64, dr[0]);
-        tmem_ld32(lane_addr + C_DP + h * 64 + 32, dr[1]);
-        tmem_ld_wait();
-        reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
-        uint32_t pk[32], dk[32];
+      for (int q4 = 0; q4 < 16; ++q4) {  // 4 query columns per step
+        const float4 l4 = lds_f4(vec + (col0 + 4 * q4) * 4);
+        const float4 d4 = lds_f4(vec + 1024 + (col0 + 4 * q4) * 4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pp[4], dd[4];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int c = h * 64 + 2 * e + t;
-            const float sv = __uint_as_float(sr[(2 * e + t) >> 5][(2 * e + t) & 31]);
-            const float dv = __uint_as_float(dr[(2 * e + t) >> 5][(2 * e + t) & 31]);
-            float pr = ex2(fmaf(sv, p.scale_log2, -sL[c] * kLog2e));
-            if (need_mask && !visible(p, m0 + c, n)) pr = 0.f;
-            pp[t] = pr;
-            dd[t] = pr * (dv - sD[c]);
-          }
-          pk[e] = pack_bf16(pp[0], pp[1]);
-          dk[e] = pack_bf16(dd[0], dd[1]);
+        for (int t = 0; t < 4; ++t) {
+          const int e = 4 * q4 + t;  // column within the group's 64
+          const float sv = __uint_as_float(sr[e >> 5][e & 31]);
+          const float dv = __uint_as_float(dr[e >> 5][e & 31]);
+          float pr = ex2(fmaf(sv, sl2, -lv[t]));
+          if (need_mask && !visible(p, m0 + col0 + e, n)) pr = 0.f;
+          pp[t] = pr;
+          dd[t] = pr * (dv - dvv[t]);
         }
-        tmem_st32(lane_addr + C_S + h * 32, pk);
-        tmem_st32(lane_addr + C_DP + h * 32, dk);
+        pk[2 * q4] = pack_bf16(pp[0], pp[1]);
+        pk[2 * q4 + 1] = pack_bf16(pp[2], pp[3]);
+        dk[2 * q4] = pack_bf16(dd[0], dd[1]);
+        dk[2 * q4 + 1] = pack_bf16(dd[2], dd[3]);
       }
+      tmem_st32(lane_addr + C_S + col0, pk);
+      tmem_st32(lane_addr + C_DP + col0, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -364,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have) have = __all_sync(0xffffffffu, mbar_wait(&o_done, 0, &abort_flag, p.status, 72));
       tc_fence_after();
       if (!abort_flag) {
-        store_rows<D>(p, lane_addr + C_DV, p.out_b, p.obs, b, hkv, n, 1.f, false, have);
-        store_rows<D>(p, lane_addr + C_DK, p.out_a, p.oas, b, hkv, n, p.scale, true, have);
+        // each group stores half of the column pairs (i, i + D/2)
+        store_rows<D>(p, lane_addr + C_DV, p.out_b, p.obs, b, hkv, n, 1.f, false, have, wg, wg + 1);
+        store_rows<D>(p, lane_addr + C_DK, p.out_a, p.oas, b, hkv, n, p.scale, true, have, wg, wg + 1);
       }
     }
   }
@@ -411,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&q_full, 1);
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(&s_full, 1);
-    mbar_init(&p_full, 4);
+    mbar_init(&p_full, 8);  // one arrival per row warp
     mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -422,7 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   reg_dealloc<kRegsControl>();
+   if (warp == kLoadWarp) {
     if (lane == 0) {
       tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
       if (iters > 0) {
@@ -433,9 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       int uses[NS] = {0, 0};
+      auto prefetch = [&](int i) {
+        if (i >= iters) return;
+        const int nk = walk.tile(i) * BT;
+        for (int a = 0; a < ATOMS; ++a) {
+          tma_prefetch_l2_4d(&tk, a * 64, nk, hkv, b);
+          tma_prefetch_l2_4d(&tv, a * 64, nk, hkv, b);
+        }
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch(i);
       for (int i = 0; i < iters; ++i) {
         const int s = i % NS;
         const int nk0 = walk.tile(i) * BT;
+        prefetch(i + kPrefetch);
         if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, &abort_flag, p.status, 81)) break;
         uint8_t* st = smem + C::qStage0 + s * C::qStage;
         mbar_arrive_expect_tx(&full[s], 2 * C::kTile);
@@ -452,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
     const uint64_t dQk = sdesc_sw128(smem_u32(smem + C::qQ), 16, 1024);
     const uint64_t dDOk = sdesc_sw128(smem_u32(smem + C::qDO), 16, 1024);
@@ -482,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dKn = sdesc_sw128(st, ATOM_BYTES, 1024);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts(tmem + C_DQ, tmem + C_S + kk * 8, dKn + (uint64_t)(kk * 2048 >> 4), ID_TS,
+          mma_ts(tmem + C_DQ, tmem + C_S + (kk >> 2) * 64 + (kk & 3) * 8, dKn + (uint64_t)(kk * 2048 >> 4), ID_TS,
                  (i > 0 || kk > 0) ? 1u : 0u);  // dQ += dS K
         mma_commit(&empty[s]);
       }
@@ -494,14 +549,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&drain, 0, 200000000ll);
     }
     __syncwarp();
+   }
   } else {
-    // ---------------- rows: warps 0-3, thread r = query row m0 + r --------
-    const int r = warp * 32 + lane;
+    reg_alloc<kRegsRows>();
+    // ---------------- rows: thread r = query row m0 + r; group wg takes the
+    // key columns 64 wg .. 64 wg + 63 of each S / dP tile --------------------
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int m = m0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int col0 = wg * 64;
     const int64_t row = ((int64_t)b * p.Hq + hq) * p.S + m;
-    const float lse_l2 = p.lse[row] * kLog2e;
+    const float lse_l2 = p.lse2[row];
     const float dsum = p.dsum[row];
+    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < iters; ++i) {
       const int nk0 = walk.tile(i) * BT;
@@ -509,32 +570,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = tile_needs_mask(p, m0, nk0);
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(lane_addr + C_S + col0, sr[0]);
+      tmem_ld32(lane_addr + C_S + col0 + 32, sr[1]);
+      tmem_ld32(lane_addr + C_DP + col0, dr[0]);
+      tmem_ld32(lane_addr + C_DP + col0 + 32, dr[1]);
+      tmem_ld_wait();
+      reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+      uint32_t dk[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // key columns 64h .. 64h + 63
-        uint32_t sr[2][32], dr[2][32];
-        tmem_ld32(lane_addr + C_S + h * 64, sr[0]);
-        tmem_ld32(lane_addr + C_S + h * 64 + 32, sr[1]);
-        tmem_ld32(lane_addr + C_DP + h * 64, dr[0]);
-        tmem_ld32(lane_addr + C_DP + h * 64 + 32, dr[1]);
-        tmem_ld_wait();
-        reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
-        uint32_t dk[32];
+      for (int e2 = 0; e2 < 32; ++e2) {
+        float dd[2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float dd[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int c = h * 64 + 2 * e + t;
-            const float sv = __uint_as_float(sr[(2 * e + t) >> 5][(2 * e + t) & 31]);
-            const float dv = __uint_as_float(dr[(2 * e + t) >> 5][(2 * e + t) & 31]);
-            float pr = ex2(fmaf(sv, p.scale_log2, -lse_l2));
-            if (need_mask && !visible(p, m, nk0 + c)) pr = 0.f;
-            dd[t] = pr * (dv - dsum);
-          }
-          dk[e] = pack_bf16(dd[0], dd[1]);
+        for (int t = 0; t < 2; ++t) {
+          const int e = 2 * e2 + t;
+          const float sv = __uint_as_float(sr[e >> 5][e & 31]);
+          const float dv = __uint_as_float(dr[e >> 5][e & 31]);
+          float pr = ex2(fmaf(sv, sl2, -lse_l2));
+          if (need_mask && !visible(p, m, nk0 + col0 + e)) pr = 0.f;
+          dd[t] = pr * (dv - dsum);
         }
-        tmem_st32(lane_addr + C_S + h * 32, dk);
+        dk[e2] = pack_bf16(dd[0], dd[1]);
       }
+      tmem_st32(lane_addr + C_S + col0, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -544,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool have = iters > 0;
       if (have) have = __all_sync(0xffffffffu, mbar_wait(&o_done, 0, &abort_flag, p.status, 102));
       tc_fence_after();
-      if (!abort_flag) store_rows<D>(p, lane_addr + C_DQ, p.out_a, p.oas, b, hq, m, p.scale, true, have);
+      if (!abort_flag) store_rows<D>(p, lane_addr + C_DQ, p.out_a, p.oas, b, hq, m, p.scale, true, have, wg, wg + 1);
     }
   }
   tc_fence_before();
@@ -555,9 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // D = rowsum(dO * O): one warp per row of [B, H, S, d].
 template <typename T>
-__global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, float* dsum, int B, int H, int S, int d,
-                                                   int64_t ds0, int64_t ds1, int64_t ds2, int64_t os0, int64_t os1,
-                                                   int64_t os2) {
+__global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, float* dsum, const float* lse,
+                                                   float* lse2, int B, int H, int S, int d, int64_t ds0, int64_t ds1,
+                                                   int64_t ds2, int64_t os0, int64_t os1, int64_t os2) {
   const int64_t rows = (int64_t)B * H * S;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -571,7 +629,10 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, fl
   for (int c = lane; c < d; c += 32) acc = fmaf(static_cast<float>(dr[c]), static_cast<float>(orow[c]), acc);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dsum[row] = acc;
+  if (lane == 0) {
+    dsum[row] = acc;
+    lse2[row] = lse[row] * kLog2e;
+  }
 }
 
 template <int D>
@@ -585,7 +646,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.S = a.S; p.group = a.Hq / a.Hkv; p.n_tiles = a.S / BT;
   p.mask = a.mask; p.sink = a.sink; p.window = a.window;
   p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;
-  p.lse = a.lse; p.dsum = a.dsum;
+  p.lse2 = a.lse2; p.dsum = a.dsum;
   p.out_bf16 = a.out_bf16;
   p.f = a.f;
   p.status = device_status_word();
@@ -611,19 +672,20 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, int B, int H, int S, int d,
-                        const int64_t ds[3], const int64_t os[3], cudaStream_t st) {
+cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, const float* lse, float* lse2, int B,
+                        int H, int S, int d, const int64_t ds[3], const int64_t os[3], cudaStream_t st) {
   const int64_t rows = (int64_t)B * H * S;
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (bf16)
     dsum_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(o), dsum, B, H, S, d, ds[0], ds[1],
-        ds[2], os[0], os[1], os[2]);
+        static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(o), dsum, lse, lse2, B, H, S, d,
+        ds[0], ds[1], ds[2], os[0], os[1], os[2]);
   else
     dsum_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float*>(dout), static_cast<const float*>(o),
-                                                         dsum, B, H, S, d, ds[0], ds[1], ds[2], os[0], os[1], os[2]);
+                                                         dsum, lse, lse2, B, H, S, d, ds[0], ds[1], ds[2], os[0], os[1],
+                                                         os[2]);
   return cudaGetLastError();
 }
 

@@ -369,7 +369,7 @@ size_t yr_bwd_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t 
   const size_t q = (size_t)B * Hq * S * d * 2, kv = (size_t)B * Hkv * S * d * 2;
   size_t bytes = align16(q) + align16(kv);                   // rotated Q, K
   if (in_dtype == YR_F32) bytes += align16(kv) + align16(q);  // bf16 V, dO
-  bytes += align16((size_t)B * Hq * S * 4);                  // D = rowsum(dO * O)
+  bytes += 2 * align16((size_t)B * Hq * S * 4);              // D = rowsum(dO * O), LSE * log2(e)
   return bytes;
 }
 
@@ -449,9 +449,11 @@ yr_status attn_bwd(const yr_rope_cfg* cfg, const void* q, const void* k, const v
   }
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd rotation pass");
   float* dsum = reinterpret_cast<float*>(ws + off);
-  e = launch_dsum(dout, o, in_dtype == YR_BF16, dsum, B, Hq, S, d, do_strides, o_strides, cs);
+  off += align16((size_t)B * Hq * S * 4);
+  float* lse2 = reinterpret_cast<float*>(ws + off);
+  e = launch_dsum(dout, o, in_dtype == YR_BF16, dsum, lse, lse2, B, Hq, S, d, do_strides, o_strides, cs);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd rowsum(dO * O)");
-  a.lse = lse; a.dsum = dsum;
+  a.lse2 = lse2; a.dsum = dsum;
   a.dq = dq; a.dk = dk; a.dv = dv; a.out_bf16 = out_dtype == YR_BF16;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.S = S; a.d = d;
   for (int i = 0; i < 3; ++i) { a.dqs[i] = dq_strides[i]; a.dks[i] = dk_strides[i]; a.dvs[i] = dv_strides[i]; }
