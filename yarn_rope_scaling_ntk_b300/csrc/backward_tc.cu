@@ -8,13 +8,16 @@
 //   P = exp(scale S - LSE),  dP = dO V^T,  dS = P * (dP - D)
 //   dV = P^T dO,  dKr = scale dS^T Qr,  dQr = scale dS Kr
 //   dk = R_n^T dKr,  dq = R_m^T dQr  (the rotation is orthogonal).
-// Two kernels, each one CTA per 128-row tile, 192 threads:
+// Two kernels, each one CTA per 128-row tile:
 //   bwd_kv_kernel: a 128-key tile of one (batch, KV head) walks the query
 //     tiles (of every query head of its group) that see it.  TMEM: S^T | dP^T
-//     | dV | dK; P^T and dS^T are written as bf16 over the first 64 columns of
-//     S^T and dP^T and feed the dV and dK products from TMEM.
-//   bwd_q_kernel: a 128-query tile walks its key tiles.  TMEM: S | dP | dQ;
-//     dS overwrites S and feeds the dQ product.
+//     | dV | dK.  Each query tile is taken as two 64-query halves with their
+//     own barriers: P^T and dS^T of a half are written as bf16 over its first
+//     32 columns of S^T and dP^T and feed its dV and dK products from TMEM,
+//     after which that half's S^T and dP^T of the next query tile are
+//     computed, while the other half's rows run.
+//   bwd_q_kernel: a 128-query tile walks its key tiles.  TMEM: S | S | dP |
+//     dQ; dS overwrites S and feeds the dQ product.
 // Roles (384 threads): warps 0-3 and 4-7 are two row groups on the same TMEM
 // lanes (thread r owns tile row r), group 0 taking columns 0-63 and group 1
 // columns 64-127 of each S / dP tile, so two warps per SM sub-partition hide
@@ -25,6 +28,8 @@
 // inverse rotation.  Every wait is bounded.
 #include <math.h>
 #include <string.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -73,12 +78,6 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
-}
-
-__device__ __forceinline__ bool visible(const BwdParams& p, int m, int n) {
-  if (p.mask == YR_MASK_NONE) return true;
-  if (n > m) return false;
-  return p.mask != YR_MASK_SINK_WINDOW || n < p.sink || m - n < p.window;
 }
 
 // Does a (query tile, key tile) pair need the element mask?
@@ -135,10 +134,10 @@ struct Cfg {
   static constexpr int kvK = 0, kvV = kTile, kvStage0 = 2 * kTile;
   static constexpr int kvStage = 2 * kTile + 2 * 1024;  // Q | dO | LSE | D (vectors padded to 1 KB)
   static constexpr int kvBytes = kvStage0 + NS * kvStage;
-  // q kernel: Q, dO once; per stage K, V
-  static constexpr int qQ = 0, qDO = kTile, qStage0 = 2 * kTile;
-  static constexpr int qStage = 2 * kTile;
-  static constexpr int qBytes = qStage0 + NS * qStage;
+  // q kernel: Q, dO once; K in three slots, V in two
+  static constexpr int qKSlots = 3, qVSlots = 2;
+  static constexpr int qQ = 0, qDO = kTile, qK0 = 2 * kTile, qV0 = qK0 + qKSlots * kTile;
+  static constexpr int qBytes = qV0 + qVSlots * kTile;
 };
 
 // Row `row` of a 128 x D fp32 TMEM block -> global, scaled by `mult` and,
@@ -207,13 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   constexpr int ATOMS = D / 64;
   constexpr int ATOM_BYTES = BT * 128;
-  constexpr uint32_t ID_SS = idesc_bf16_f32(BT, BT, false);  // [128 x D] x [128 x D]^T
-  constexpr uint32_t ID_TS = idesc_bf16_f32(BT, D, true);    // TMEM [128 x 128] x smem [128 x D]
+  constexpr uint32_t ID_SSH = idesc_bf16_f32(BT, BT / 2, false);  // [128 x D] x [64 x D]^T
+  constexpr uint32_t ID_TS = idesc_bf16_f32(BT, D, true);         // TMEM [128 x 16] x smem [16 x D]
   constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, full[NS], empty[NS], s_full, p_full, o_done, drain;
+  __shared__ uint64_t kv_full, full[NS], empty[NS], s_full[2], p_full[2], o_done, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -232,8 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     mbar_init(&kv_full, 1);
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, 8);  // one arrival per row warp
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 4);  // one arrival per warp of the half's row group
+    }
     mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -303,37 +304,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
     };
+    // S^T and dP^T of query half h (64 queries) of iteration i: N = 64
+    auto issue_sdp = [&](int i, int h) {
+      const uint32_t st = smem_u32(smem + C::kvStage0 + (i % NS) * C::kvStage) + h * (BT / 2) * 128;
+      const uint64_t dQk = sdesc_sw128(st, 16, 1024), dDOk = sdesc_sw128(st + C::kTile, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + C_S + 64 * h, dK + off, dQk + off, ID_SSH, kk > 0);     // S^T = K Q^T
+        mma_ss(tmem + C_DP + 64 * h, dV + off, dDOk + off, ID_SSH, kk > 0);   // dP^T = V dO^T
+      }
+      mma_commit(&s_full[h]);
+    };
+    // dV += P^T dO and dK += dS^T Q over the 64 queries of half h
+    auto issue_dvdk = [&](int i, int h) {
+      const uint32_t st = smem_u32(smem + C::kvStage0 + (i % NS) * C::kvStage);
+      const uint64_t dQn = sdesc_sw128(st, ATOM_BYTES, 1024), dDOn = sdesc_sw128(st + C::kTile, ATOM_BYTES, 1024);
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int kk = 4 * h + kq;  // 16-query step within the tile
+        const uint64_t off = (uint64_t)(kk * 2048 >> 4);
+        const uint32_t a_off = 64 * h + kq * 8;  // the half's packed bf16 columns
+        mma_ts(tmem + C_DV, tmem + C_S + a_off, dDOn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_ts(tmem + C_DK, tmem + C_DP + a_off, dQn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+    };
     bool ok = iters == 0 || wait(&kv_full, 0, 61);
+    if (ok && iters > 0) {
+      ok = wait(&full[0], 0, 62);
+      tc_fence_after();
+      if (ok && leader) { issue_sdp(0, 0); issue_sdp(0, 1); }
+      __syncwarp();
+    }
+    // per half: its dV/dK products of iteration i, then its S^T/dP^T of
+    // iteration i + 1 (into the columns those products have just read; the
+    // tensor pipe runs a CTA's MMAs in issue order), so one row group's
+    // softmax overlaps the other half's products
     for (int i = 0; ok && i < iters; ++i) {
       const int s = i % NS;
-      const uint32_t st = smem_u32(smem + C::kvStage0 + s * C::kvStage);
-      if (!wait(&full[s], (i / NS) & 1, 62)) { ok = false; break; }
-      tc_fence_after();
-      if (leader) {
-        const uint64_t dQk = sdesc_sw128(st, 16, 1024), dDOk = sdesc_sw128(st + C::kTile, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + C_S, dK + off, dQk + off, ID_SS, kk > 0);      // S^T = K Q^T
-          mma_ss(tmem + C_DP, dV + off, dDOk + off, ID_SS, kk > 0);    // dP^T = V dO^T
+      for (int h = 0; h < 2; ++h) {
+        if (!wait(&p_full[h], i & 1, 63 + h)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          issue_dvdk(i, h);
+          if (h == 1) mma_commit(&empty[s]);
         }
-        mma_commit(&s_full);
-      }
-      __syncwarp();
-      if (!wait(&p_full, i & 1, 63)) { ok = false; break; }
-      tc_fence_after();
-      if (leader) {
-        const uint64_t dQn = sdesc_sw128(st, ATOM_BYTES, 1024), dDOn = sdesc_sw128(st + C::kTile, ATOM_BYTES, 1024);
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk) {
-          const uint64_t off = (uint64_t)(kk * 2048 >> 4);
-          const uint32_t a_off = (kk >> 2) * 64 + (kk & 3) * 8;  // group (kk / 4)'s packed columns
-          mma_ts(tmem + C_DV, tmem + C_S + a_off, dDOn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dO
-          mma_ts(tmem + C_DK, tmem + C_DP + a_off, dQn + off, ID_TS, (i > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T Q
+        __syncwarp();
+        if (i + 1 < iters) {
+          if (h == 0 && !wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1, 62)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) issue_sdp(i + 1, h);
+          __syncwarp();
         }
-        mma_commit(&empty[s]);
       }
-      __syncwarp();
     }
     if (leader) {
       mma_commit(&o_done);
@@ -344,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
    }
   } else {
     reg_alloc<kRegsRows>();
-    // ---------------- rows: thread r = key row n0 + r; group wg takes the
-    // query columns 64 wg .. 64 wg + 63 of each S^T / dP^T tile ---------------
+    // ---------------- rows: thread r = key row n0 + r; group wg takes query
+    // half wg (columns 64 wg .. 64 wg + 63) of each S^T / dP^T tile ---------
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int n = n0 + r;
@@ -357,10 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % NS;
       const int m0 = (qlo + i % per_head) * BT;
       const uint32_t vec = smem_u32(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);  // LSE*log2e | D
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full, i & 1, &abort_flag, p.status, 71));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], i & 1, &abort_flag, p.status, 71));
       // the LSE / D vectors of this stage landed with full[s] (already
       // complete: the MMA waited for it before the products of s_full); the
-      // stage is refilled only after both groups' p_full below
+      // stage is refilled only after both halves' products have run
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / NS) & 1, &abort_flag, p.status, 73));
       if (!ok) break;
       tc_fence_after();
@@ -372,34 +395,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_addr + C_DP + col0 + 32, dr[1]);
       tmem_ld_wait();
       reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+      // Visible columns of key row n: e >= e_lo (causal: query m0 + col0 + e
+      // >= n) and, for a non-sink key under the window, e < e_hi.  The
+      // masked and unmasked loops are separate copies: a per-element test
+      // on the tile flag costs more than the whole unmasked pass.
+      const int e_lo = n - (m0 + col0);
+      const int e_hi = (p.mask == YR_MASK_SINK_WINDOW && n >= p.sink) ? n + p.window - (m0 + col0) : BT;
       uint32_t pk[32], dk[32];
+      auto softmax = [&](auto masked) {
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {  // 4 query columns per step
-        const float4 l4 = lds_f4(vec + (col0 + 4 * q4) * 4);
-        const float4 d4 = lds_f4(vec + 1024 + (col0 + 4 * q4) * 4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pp[4], dd[4];
+        for (int q4 = 0; q4 < 16; ++q4) {  // 4 query columns per step
+          const float4 l4 = lds_f4(vec + (col0 + 4 * q4) * 4);
+          const float4 d4 = lds_f4(vec + 1024 + (col0 + 4 * q4) * 4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], dd[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int e = 4 * q4 + t;  // column within the group's 64
-          const float sv = __uint_as_float(sr[e >> 5][e & 31]);
-          const float dv = __uint_as_float(dr[e >> 5][e & 31]);
-          float pr = ex2(fmaf(sv, sl2, -lv[t]));
-          if (need_mask && !visible(p, m0 + col0 + e, n)) pr = 0.f;
-          pp[t] = pr;
-          dd[t] = pr * (dv - dvv[t]);
+          for (int t = 0; t < 4; ++t) {
+            const int e = 4 * q4 + t;  // column within the group's 64
+            const float sv = __uint_as_float(sr[e >> 5][e & 31]);
+            const float dv = __uint_as_float(dr[e >> 5][e & 31]);
+            float pr = ex2(fmaf(sv, sl2, -lv[t]));
+            if (decltype(masked)::value && (e < e_lo || e >= e_hi)) pr = 0.f;
+            pp[t] = pr;
+            dd[t] = pr * (dv - dvv[t]);
+          }
+          pk[2 * q4] = pack_bf16(pp[0], pp[1]);
+          pk[2 * q4 + 1] = pack_bf16(pp[2], pp[3]);
+          dk[2 * q4] = pack_bf16(dd[0], dd[1]);
+          dk[2 * q4 + 1] = pack_bf16(dd[2], dd[3]);
         }
-        pk[2 * q4] = pack_bf16(pp[0], pp[1]);
-        pk[2 * q4 + 1] = pack_bf16(pp[2], pp[3]);
-        dk[2 * q4] = pack_bf16(dd[0], dd[1]);
-        dk[2 * q4 + 1] = pack_bf16(dd[2], dd[3]);
-      }
+      };
+      if (need_mask) softmax(std::true_type{});
+      else softmax(std::false_type{});
       tmem_st32(lane_addr + C_S + col0, pk);
       tmem_st32(lane_addr + C_DP + col0, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) mbar_arrive(&p_full[wg]);
     }
     if (__all_sync(0xffffffffu, ok && !abort_flag)) {
       bool have = iters > 0;
@@ -420,6 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // dQ: one CTA per (query tile, batch, query head); heaviest query tiles first.
+// TMEM: S[0] | S[1] | dP | dQ.  S is double-buffered, so S(i + 1) is computed
+// while the rows work on iteration i; dP(i + 1) waits only until the rows have
+// read dP(i) into registers.  K has three shared-memory slots (read by S and
+// dQ) and V two (read by dP alone), so the load of a later tile never waits
+// for the products of the current one.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -430,11 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int ATOM_BYTES = BT * 128;
   constexpr uint32_t ID_SS = idesc_bf16_f32(BT, BT, false);
   constexpr uint32_t ID_TS = idesc_bf16_f32(BT, D, true);
-  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+  constexpr uint32_t C_S0 = 0, C_DP = 256, C_DQ = 384;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, full[NS], empty[NS], s_full, p_full, o_done, drain;
+  __shared__ uint64_t q_full, k_full[C::qKSlots], k_empty[C::qKSlots], v_full[C::qVSlots], v_empty[C::qVSlots];
+  __shared__ uint64_t s_full[2], dp_free, p_full[2], o_done, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -452,9 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
-    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, 8);  // one arrival per row warp
+    for (int s = 0; s < C::qKSlots; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < C::qVSlots; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&dp_free, 8);  // one arrival per row warp
+    // p_full alternates with the S buffer: the rows may finish iteration i + 1
+    // before the MMA warp has seen iteration i complete
+    mbar_init(&p_full[0], 8);
+    mbar_init(&p_full[1], 8);
     mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -477,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + C::qDO + a * ATOM_BYTES, &tdo, &q_full, a * 64, m0, hq, b);
         }
       }
-      int uses[NS] = {0, 0};
+      int kuses[C::qKSlots] = {}, vuses[C::qVSlots] = {};
       auto prefetch = [&](int i) {
         if (i >= iters) return;
         const int nk = walk.tile(i) * BT;
@@ -488,22 +533,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int i = 0; i < kPrefetch; ++i) prefetch(i);
       for (int i = 0; i < iters; ++i) {
-        const int s = i % NS;
+        const int ks = i % C::qKSlots, vs = i % C::qVSlots;
         const int nk0 = walk.tile(i) * BT;
         prefetch(i + kPrefetch);
-        if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, &abort_flag, p.status, 81)) break;
-        uint8_t* st = smem + C::qStage0 + s * C::qStage;
-        mbar_arrive_expect_tx(&full[s], 2 * C::kTile);
-        for (int a = 0; a < ATOMS; ++a) {
-          tma_load_4d(st + a * ATOM_BYTES, &tk, &full[s], a * 64, nk0, hkv, b);
-          tma_load_4d(st + C::kTile + a * ATOM_BYTES, &tv, &full[s], a * 64, nk0, hkv, b);
-        }
-        ++uses[s];
+        if (!mbar_wait(&k_empty[ks], ((i / C::qKSlots) & 1) ^ 1, &abort_flag, p.status, 81)) break;
+        uint8_t* kd = smem + C::qK0 + ks * C::kTile;
+        mbar_arrive_expect_tx(&k_full[ks], C::kTile);
+        for (int a = 0; a < ATOMS; ++a) tma_load_4d(kd + a * ATOM_BYTES, &tk, &k_full[ks], a * 64, nk0, hkv, b);
+        ++kuses[ks];
+        if (!mbar_wait(&v_empty[vs], ((i / C::qVSlots) & 1) ^ 1, &abort_flag, p.status, 82)) break;
+        uint8_t* vd = smem + C::qV0 + vs * C::kTile;
+        mbar_arrive_expect_tx(&v_full[vs], C::kTile);
+        for (int a = 0; a < ATOMS; ++a) tma_load_4d(vd + a * ATOM_BYTES, &tv, &v_full[vs], a * 64, nk0, hkv, b);
+        ++vuses[vs];
       }
       if (abort_flag) {
         if (iters > 0) mbar_wait_drain(&q_full, 0, 200000000ll);
-        for (int s = 0; s < NS; ++s)
-          if (uses[s]) mbar_wait_drain(&full[s], (uses[s] - 1) & 1, 200000000ll);
+        for (int s = 0; s < C::qKSlots; ++s)
+          if (kuses[s]) mbar_wait_drain(&k_full[s], (kuses[s] - 1) & 1, 200000000ll);
+        for (int s = 0; s < C::qVSlots; ++s)
+          if (vuses[s]) mbar_wait_drain(&v_full[s], (vuses[s] - 1) & 1, 200000000ll);
       }
     }
     __syncwarp();
@@ -514,32 +563,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
     };
-    bool ok = iters == 0 || wait(&q_full, 0, 91);
-    for (int i = 0; ok && i < iters; ++i) {
-      const int s = i % NS;
-      const uint32_t st = smem_u32(smem + C::qStage0 + s * C::qStage);
-      if (!wait(&full[s], (i / NS) & 1, 92)) { ok = false; break; }
-      tc_fence_after();
-      if (leader) {
-        const uint64_t dKk = sdesc_sw128(st, 16, 1024), dVk = sdesc_sw128(st + C::kTile, 16, 1024);
+    auto k_addr = [&](int i) { return smem_u32(smem + C::qK0 + (i % C::qKSlots) * C::kTile); };
+    auto v_addr = [&](int i) { return smem_u32(smem + C::qV0 + (i % C::qVSlots) * C::kTile); };
+    auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into S[i & 1]
+      const uint64_t dKk = sdesc_sw128(k_addr(i), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + C_S, dQk + off, dKk + off, ID_SS, kk > 0);     // S = Q K^T
-          mma_ss(tmem + C_DP, dDOk + off, dVk + off, ID_SS, kk > 0);   // dP = dO V^T
-        }
-        mma_commit(&s_full);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + C_S0 + 128 * (i & 1), dQk + off, dKk + off, ID_SS, kk > 0);
       }
+    };
+    auto issue_dp = [&](int i) {  // dP(i) = dO V(i)^T
+      const uint64_t dVk = sdesc_sw128(v_addr(i), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + C_DP, dDOk + off, dVk + off, ID_SS, kk > 0);
+      }
+      mma_commit(&v_empty[i % C::qVSlots]);
+      mma_commit(&s_full[i & 1]);
+    };
+    bool ok = iters == 0 || wait(&q_full, 0, 91);
+    if (ok && iters > 0) {
+      ok = wait(&k_full[0], 0, 92) && wait(&v_full[0], 0, 94);
+      tc_fence_after();
+      if (ok && leader) { issue_s(0); issue_dp(0); }
       __syncwarp();
-      if (!wait(&p_full, i & 1, 93)) { ok = false; break; }
+    }
+    for (int i = 0; ok && i < iters; ++i) {
+      if (i + 1 < iters) {
+        const int j = i + 1;
+        if (!wait(&k_full[j % C::qKSlots], (j / C::qKSlots) & 1, 92)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) issue_s(j);  // the other S buffer: dQ(i - 1) read it and was issued before
+        __syncwarp();
+        if (!wait(&v_full[j % C::qVSlots], (j / C::qVSlots) & 1, 94) || !wait(&dp_free, i & 1, 95)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (leader) issue_dp(j);
+        __syncwarp();
+      }
+      if (!wait(&p_full[i & 1], (i >> 1) & 1, 93)) { ok = false; break; }
       tc_fence_after();
       if (leader) {
-        const uint64_t dKn = sdesc_sw128(st, ATOM_BYTES, 1024);
+        const uint64_t dKn = sdesc_sw128(k_addr(i), ATOM_BYTES, 1024);
+        const uint32_t a0 = tmem + C_S0 + 128 * (i & 1);
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts(tmem + C_DQ, tmem + C_S + (kk >> 2) * 64 + (kk & 3) * 8, dKn + (uint64_t)(kk * 2048 >> 4), ID_TS,
+          mma_ts(tmem + C_DQ, a0 + (kk >> 2) * 64 + (kk & 3) * 8, dKn + (uint64_t)(kk * 2048 >> 4), ID_TS,
                  (i > 0 || kk > 0) ? 1u : 0u);  // dQ += dS K
-        mma_commit(&empty[s]);
+        mma_commit(&k_empty[i % C::qKSlots]);
       }
       __syncwarp();
     }
@@ -566,37 +641,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = 0; i < iters; ++i) {
       const int nk0 = walk.tile(i) * BT;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full, i & 1, &abort_flag, p.status, 101));
+      const uint32_t c_s = C_S0 + 128 * (i & 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i & 1], (i >> 1) & 1, &abort_flag, p.status, 101));
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = tile_needs_mask(p, m0, nk0);
       uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(lane_addr + C_S + col0, sr[0]);
-      tmem_ld32(lane_addr + C_S + col0 + 32, sr[1]);
+      tmem_ld32(lane_addr + c_s + col0, sr[0]);
+      tmem_ld32(lane_addr + c_s + col0 + 32, sr[1]);
       tmem_ld32(lane_addr + C_DP + col0, dr[0]);
       tmem_ld32(lane_addr + C_DP + col0 + 32, dr[1]);
       tmem_ld_wait();
       reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dp_free);  // dP(i) is in registers: dP(i + 1) may overwrite it
+      // Visible columns of query row m (key nk0 + col0 + e): e <= e_max
+      // (causal) and, under the window, a sink key (e < e_sink) or one
+      // inside the window (e > e_win).  Masked and unmasked loops are
+      // separate copies, as in the dK/dV kernel.
+      const int base = nk0 + col0;
+      const bool sw = p.mask == YR_MASK_SINK_WINDOW;
+      const int e_max = m - base;
+      const int e_sink = sw ? p.sink - base : BT;
+      const int e_win = sw ? m - p.window - base : -1;
       uint32_t dk[32];
+      auto softmax = [&](auto masked) {
 #pragma unroll
-      for (int e2 = 0; e2 < 32; ++e2) {
-        float dd[2];
+        for (int e2 = 0; e2 < 32; ++e2) {
+          float dd[2];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int e = 2 * e2 + t;
-          const float sv = __uint_as_float(sr[e >> 5][e & 31]);
-          const float dv = __uint_as_float(dr[e >> 5][e & 31]);
-          float pr = ex2(fmaf(sv, sl2, -lse_l2));
-          if (need_mask && !visible(p, m, nk0 + col0 + e)) pr = 0.f;
-          dd[t] = pr * (dv - dsum);
+          for (int t = 0; t < 2; ++t) {
+            const int e = 2 * e2 + t;
+            const float sv = __uint_as_float(sr[e >> 5][e & 31]);
+            const float dv = __uint_as_float(dr[e >> 5][e & 31]);
+            float pr = ex2(fmaf(sv, sl2, -lse_l2));
+            if (decltype(masked)::value && (e > e_max || (e >= e_sink && e <= e_win))) pr = 0.f;
+            dd[t] = pr * (dv - dsum);
+          }
+          dk[e2] = pack_bf16(dd[0], dd[1]);
         }
-        dk[e2] = pack_bf16(dd[0], dd[1]);
-      }
-      tmem_st32(lane_addr + C_S + col0, dk);
+      };
+      if (need_mask) softmax(std::true_type{});
+      else softmax(std::false_type{});
+      tmem_st32(lane_addr + c_s + col0, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
     }
     if (__all_sync(0xffffffffu, ok && !abort_flag)) {
       bool have = iters > 0;
