@@ -45,6 +45,9 @@ KERNEL_SOURCES = {
     "prefill_tc": ("prefill_tc.cu", "tc_ptx.cuh"),
     "decode": ("decode.cu", "tc_ptx.cuh", "common.cuh"),
     "rope": ("rope.cu", "common.cuh"),
+    "decode_fp8": ("decode.cu", "tc_ptx.cuh", "common.cuh"),
+    "bwd_kv": ("backward_tc.cu", "tc_ptx.cuh", "common.cuh"),
+    "bwd_q": ("backward_tc.cu", "tc_ptx.cuh", "common.cuh"),
 }
 TRAFFIC = {
     # kernel: (source hash, bytes per launch, what was captured)
@@ -429,7 +432,8 @@ def run_ours(args):
         bflops = 2.5 * prefill_flops(w)
         bwd = {"workload": w.name, "ms": bwd_ms, "TFLOP/s": bflops / (bwd_ms * 1e-3) / 1e12,
                "frac_of_burst": bflops / (bwd_ms * 1e-3) / 1e12 / tf_burst,
-               "flops": "10 d per visible pair (the kernels do 14 d: S and dP are recomputed in both)"}
+               "flops": "10 d per visible pair (the kernels do 14 d: S and dP are recomputed in both)",
+               "traffic_per_launch": {"bwd_kv_kernel": traffic("bwd_kv"), "bwd_q_kernel": traffic("bwd_q")}}
         del qb, kb, vb, ob, lseb, dob, bws
         torch.cuda.empty_cache()
 
@@ -470,7 +474,7 @@ def run_ours(args):
         "decode_fp8": {"workload": wd.name + "_fp8_e4m3", "value": dec8_gbs, "unit": "GB/s", "ms": dec8_ms,
                        "speedup_vs_bf16_cache": dec_ms / dec8_ms,
                        "roofline": {"bound": "hbm", "achieved": dec8_gbs, "peak": hbm, "unit": "GB/s",
-                                    "frac": dec8_gbs / hbm, "traffic": None}},
+                                    "frac": dec8_gbs / hbm, "traffic": traffic("decode_fp8")}},
         "backward": bwd,
         "other_prefill_workloads": others,
         "rope_apply": {"workload": "Q and K of " + w.name, "value": rope_gbs, "unit": "GB/s",
@@ -489,7 +493,7 @@ def run_ours(args):
 
 
 def run_part(args):
-    """One kernel family alone, for profiling: ``--part prefill|decode|rope``
+    """One kernel family alone, for profiling: ``--part prefill|decode|decode_fp8|rope|backward``
     runs W + K calls of that entry point; ``--small`` shrinks the workload
     (prefill S=4096, decode B=8) while keeping inputs larger than L2."""
     from dataclasses import replace
@@ -518,6 +522,12 @@ def run_part(args):
                 api.attn_fwd_prefill(cfg, q, k, v, mask=w.mask, out=o, workspace=ws)
             else:
                 api.rope_apply(cfg, q, out=o)
+    elif args.part == "decode_fp8":
+        wd = W.DECODE if not args.small else replace(W.DECODE, B=8, name="decode_B8")
+        dq, kc, vc, ks, vs, nv, rs = W.decode_inputs_fp8(wd, dev)
+        dcfg = api.RopeConfig(kind="plain", head_dim=wd.d, theta_base=wd.rope.theta_base)
+        for _ in range(n):
+            api.attn_fwd_decode_sinkwindow_fp8(dcfg, dq, kc, vc, ks, vs, nv, rs, wd.sink, wd.window)
     else:
         wd = W.DECODE if not args.small else replace(W.DECODE, B=8, name="decode_B8")
         dq, kc, vc, nv, rs = W.decode_inputs(wd, dev)
@@ -538,7 +548,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip timing the attention backward")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the ring 128K and GQA prefill workloads")
-    ap.add_argument("--part", choices=["prefill", "decode", "rope", "backward"], default=None,
+    ap.add_argument("--part", choices=["prefill", "decode", "decode_fp8", "rope", "backward"], default=None,
                     help="profile one kernel family alone (prints no bench line)")
     ap.add_argument("--small", action="store_true", help="with --part: smaller workload")
     args = ap.parse_args()
