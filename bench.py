@@ -51,12 +51,18 @@ KERNEL_SOURCES = {
 }
 TRAFFIC = {
     # kernel: (source hash, bytes per launch, what was captured)
-    "prefill_tc": ("e12dd2ec64287794", 510.50e6 + 117.03e6,
+    "prefill_tc": ("ef5cbaad609205d0", 510.16e6 + 118.21e6,
                    "bench.py --part prefill: Llama-2-7B shape S=16384, one launch"),
-    "decode": ("ba6d6bf8234c171d", 4.30e9 + 3.59e6,
+    "decode": ("175b125d7157b292", 4.30e9 + 3.57e6,
                "bench.py --part decode: 64 sequences x 32 heads x 4096 slots, one launch"),
-    "rope": ("9ff39cab7d064477", 134.24e6 + 89.90e6,
+    "decode_fp8": ("175b125d7157b292", 2.15e9 + 3.54e6,
+                   "bench.py --part decode_fp8: the same cache shape in FP8 E4M3, one launch"),
+    "rope": ("b80e2ddfaa08bdd0", 134.24e6 + 89.69e6,
              "bench.py --part rope: Q [1, 32, 16384, 128] bf16, one launch"),
+    "bwd_kv": ("ecd0a5c84e4bee9c", 550.20e6 + 240.68e6,
+               "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
+    "bwd_q": ("ecd0a5c84e4bee9c", 557.30e6 + 116.45e6,
+              "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
 }
 
 

@@ -29,6 +29,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -54,6 +55,7 @@ constexpr int kPrefetch = 4;   // iterations whose tiles the producer prefetches
 
 struct BwdParams {
   int B, Hq, Hkv, S, group, n_tiles;
+  int hgroup;        // heads per scheduling group
   int mask, sink, window;
   float scale_log2;  // scale * log2(e)
   float scale;       // softmax scale (applied to dQ and dK)
@@ -78,6 +80,27 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
+}
+
+// CTA i of a grid of U units (batch x head) x n_tiles tiles, taken in groups
+// of hg units: every tile of a group before the next group, tile-major inside
+// a group, so the CTAs resident at once share a few heads and the tiles they
+// all re-read (Q and dO, or K and V) stay in L2.
+__device__ __forceinline__ void sched_unit(int i, int U, int n_tiles, int hg, int& tile, int& unit) {
+  const int per_group = hg * n_tiles;
+  const int full = U / hg;
+  int g, r, hc;
+  if (i < full * per_group) {
+    g = i / per_group;
+    r = i - g * per_group;
+    hc = hg;
+  } else {
+    g = full;
+    r = i - full * per_group;
+    hc = U - full * hg;
+  }
+  tile = r / hc;
+  unit = g * hg + r % hc;
 }
 
 // Does a (query tile, key tile) pair need the element mask?
@@ -196,8 +219,8 @@ __device__ __forceinline__ void store_rows(const BwdParams& p, uint32_t taddr, v
 }
 
 // ---------------------------------------------------------------------------
-// dK, dV: one CTA per (key tile, batch, KV head); key tiles ascending (the
-// causal tiles with the most query tiles first).
+// dK, dV: one CTA per (key tile, batch, KV head); in each scheduling group key
+// tiles ascending (the causal tiles with the most query tiles first).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -217,9 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BH = p.B * p.Hkv;
-  const int kt = (int)(blockIdx.x / BH);
-  const int bkv = blockIdx.x % BH;
+  int kt, bkv;
+  sched_unit((int)blockIdx.x, p.B * p.Hkv, p.n_tiles, p.hgroup, kt, bkv);
   const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
   const int n0 = kt * BT;
   int qlo, qhi;
@@ -452,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ: one CTA per (query tile, batch, query head); heaviest query tiles first.
+// dQ: one CTA per (query tile, batch, query head); in each scheduling group the
+// heaviest query tiles first.
 // TMEM: S[0] | S[1] | dP | dQ.  S is double-buffered, so S(i + 1) is computed
 // while the rows work on iteration i; dP(i + 1) waits only until the rows have
 // read dP(i) into registers.  K has three shared-memory slots (read by S and
@@ -478,9 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BH = p.B * p.Hq;
-  const int qt = p.n_tiles - 1 - (int)(blockIdx.x / BH);
-  const int bh = blockIdx.x % BH;
+  int t, bh;
+  sched_unit((int)blockIdx.x, p.B * p.Hq, p.n_tiles, p.hgroup, t, bh);
+  const int qt = p.n_tiles - 1 - t;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int hkv = hq / p.group;
   const int m0 = qt * BT;
@@ -744,7 +767,10 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
   p.status = device_status_word();
   if (!p.status) return cudaErrorInvalidValue;
   using C = Cfg<D>;
+  // about four waves of CTAs per scheduling group
+  auto heads_per_group = [&](int units) { return std::max(1, std::min(units, (4 * sm_count() + p.n_tiles - 1) / p.n_tiles)); };
   // dK, dV
+  p.hgroup = heads_per_group(a.B * a.Hkv);
   p.out_a = a.dk; p.out_b = a.dv;
   for (int i = 0; i < 3; ++i) { p.oas[i] = a.dks[i]; p.obs[i] = a.dvs[i]; }
   int smem = C::kvBytes + 1024;
@@ -753,6 +779,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
   bwd_kv_kernel<D><<<(unsigned)(p.n_tiles * a.B * a.Hkv), kThreads, smem, st>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // dQ
+  p.hgroup = heads_per_group(a.B * a.Hq);
   p.out_a = a.dq; p.out_b = nullptr;
   for (int i = 0; i < 3; ++i) p.oas[i] = a.dqs[i];
   smem = C::qBytes + 1024;
