@@ -101,6 +101,22 @@ __device__ __forceinline__ void load_cache(const uint8_t* p, float (&x)[N]) {
   else load_e4m3<N>(p, x);
 }
 
+// Two float32 lanes at once (sm_100 family packed arithmetic); each lane is
+// an ordinary round-to-nearest float32 fma / multiply.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -219,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
     if (identity) { stc[k] = 1.f; sts[k] = 0.f; }
     else turn_cos_sin<false>((float)KPS, fr[k], stc[k], sts[k]);
   }
+  float nsts[PPT];
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) nsts[k] = -sts[k];
   {
     float cs[PPT], sn[PPT];
 #pragma unroll
@@ -290,63 +309,100 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       load_cache<PPT, EB>(kr + HALF * EB, x2);
       load_cache<PPT, EB>(vr, y1);
       load_cache<PPT, EB>(vr + HALF * EB, y2);
-      float kr1[PPT], kr2[PPT];   // key as dotted: raw (kRotQ) or rotated at j
-      float qa1[G][PPT], qa2[G][PPT];
-      if (!kRecur && !identity) {
+      if constexpr (kRotQ) {
+        // raw key against the backward-rotated query, two pairs per packed op
+        float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < PPT; ++k) turn_cos_sin<false>((float)j, fr[k], rc[k], rs_[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < PPT; ++k) {
-        if (kRotQ) {
-          kr1[k] = x1[k];
-          kr2[k] = x2[k];
-          qa1[0][k] = qh1[k];
-          qa2[0][k] = qh2[k];
+        for (int k = 0; k < PPT; k += 2) {
+          fma2(d0, d1, qh1[k], qh1[k + 1], x1[k], x1[k + 1], d0, d1);
+          fma2(d0, d1, qh2[k], qh2[k + 1], x2[k], x2[k + 1], d0, d1);
           // next key: q_hat <- R(-KPS theta) q_hat
-          const float a1 = qh1[k], a2 = qh2[k];
-          qh1[k] = a1 * stc[k] + a2 * sts[k];
-          qh2[k] = a2 * stc[k] - a1 * sts[k];
-        } else {
-          kr1[k] = x1[k] * rc[k] - x2[k] * rs_[k];
-          kr2[k] = x1[k] * rs_[k] + x2[k] * rc[k];
-#pragma unroll
-          for (int g = 0; g < G; ++g) { qa1[g][k] = q1[g][k]; qa2[g][k] = q2[g][k]; }
+          float n1a, n1b, n2a, n2b;
+          mul2(n1a, n1b, qh2[k], qh2[k + 1], sts[k], sts[k + 1]);
+          fma2(n1a, n1b, qh1[k], qh1[k + 1], stc[k], stc[k + 1], n1a, n1b);
+          mul2(n2a, n2b, qh1[k], qh1[k + 1], nsts[k], nsts[k + 1]);
+          fma2(n2a, n2b, qh2[k], qh2[k + 1], stc[k], stc[k + 1], n2a, n2b);
+          qh1[k] = n1a; qh1[k + 1] = n1b; qh2[k] = n2a; qh2[k + 1] = n2b;
         }
-        // advance to the thread's next key: (m - j) decreases (kRotQ) or j
-        // increases by KPS
-        if (kRecur && !kRotQ) {
-          const float c0 = rc[k], s0 = rs_[k];
-          rc[k] = c0 * stc[k] - s0 * sts[k];
-          rs_[k] = s0 * stc[k] + c0 * sts[k];
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float dot = 0.f;
-#pragma unroll
-        for (int k = 0; k < PPT; ++k) dot = fmaf(qa1[g][k], kr1[k], fmaf(qa2[g][k], kr2[k], dot));
+        float dot = d0 + d1;
 #pragma unroll
         for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (EB == 1) dot *= k_scale;
+        dot *= k_scale;
         if (valid) {
-          if (dot > mrun[g] + kRescaleThreshold) {  // lazy: the reference moves rarely
-            const float corr = exp2_diff(mrun[g], dot);
-            lrun[g] *= corr;
+          if (dot > mrun[0] + kRescaleThreshold) {  // lazy: the reference moves rarely
+            const float corr = exp2_diff(mrun[0], dot);
+            lrun[0] *= corr;
 #pragma unroll
-            for (int k = 0; k < PPT; ++k) { acc1[g][k] *= corr; acc2[g][k] *= corr; }
-            mrun[g] = dot;
+            for (int k = 0; k < PPT; ++k) { acc1[0][k] *= corr; acc2[0][k] *= corr; }
+            mrun[0] = dot;
           }
-          const float pr = exp2f(dot - mrun[g]);
-          lrun[g] += pr;
+          const float pr = exp2f(dot - mrun[0]);
+          lrun[0] += pr;
 #pragma unroll
-          for (int k = 0; k < PPT; ++k) {
-            acc1[g][k] = fmaf(pr, y1[k], acc1[g][k]);
-            acc2[g][k] = fmaf(pr, y2[k], acc2[g][k]);
+          for (int k = 0; k < PPT; k += 2) {
+            fma2(acc1[0][k], acc1[0][k + 1], pr, pr, y1[k], y1[k + 1], acc1[0][k], acc1[0][k + 1]);
+            fma2(acc2[0][k], acc2[0][k + 1], pr, pr, y2[k], y2[k + 1], acc2[0][k], acc2[0][k + 1]);
+          }
+        }
+      } else {
+        float kr1[PPT], kr2[PPT];   // key as dotted: raw (kRotQ) or rotated at j
+        float qa1[G][PPT], qa2[G][PPT];
+        if (!kRecur && !identity) {
+  #pragma unroll
+          for (int k = 0; k < PPT; ++k) turn_cos_sin<false>((float)j, fr[k], rc[k], rs_[k]);
+        }
+  #pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+          if (kRotQ) {
+            kr1[k] = x1[k];
+            kr2[k] = x2[k];
+            qa1[0][k] = qh1[k];
+            qa2[0][k] = qh2[k];
+            // next key: q_hat <- R(-KPS theta) q_hat
+            const float a1 = qh1[k], a2 = qh2[k];
+            qh1[k] = a1 * stc[k] + a2 * sts[k];
+            qh2[k] = a2 * stc[k] - a1 * sts[k];
+          } else {
+            kr1[k] = x1[k] * rc[k] - x2[k] * rs_[k];
+            kr2[k] = x1[k] * rs_[k] + x2[k] * rc[k];
+  #pragma unroll
+            for (int g = 0; g < G; ++g) { qa1[g][k] = q1[g][k]; qa2[g][k] = q2[g][k]; }
+          }
+          // advance to the thread's next key: (m - j) decreases (kRotQ) or j
+          // increases by KPS
+          if (kRecur && !kRotQ) {
+            const float c0 = rc[k], s0 = rs_[k];
+            rc[k] = c0 * stc[k] - s0 * sts[k];
+            rs_[k] = s0 * stc[k] + c0 * sts[k];
+          }
+        }
+  #pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float dot = 0.f;
+  #pragma unroll
+          for (int k = 0; k < PPT; ++k) dot = fmaf(qa1[g][k], kr1[k], fmaf(qa2[g][k], kr2[k], dot));
+  #pragma unroll
+          for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          if (EB == 1) dot *= k_scale;
+          if (valid) {
+            if (dot > mrun[g] + kRescaleThreshold) {  // lazy: the reference moves rarely
+              const float corr = exp2_diff(mrun[g], dot);
+              lrun[g] *= corr;
+  #pragma unroll
+              for (int k = 0; k < PPT; ++k) { acc1[g][k] *= corr; acc2[g][k] *= corr; }
+              mrun[g] = dot;
+            }
+            const float pr = exp2f(dot - mrun[g]);
+            lrun[g] += pr;
+  #pragma unroll
+            for (int k = 0; k < PPT; ++k) {
+              acc1[g][k] = fmaf(pr, y1[k], acc1[g][k]);
+              acc2[g][k] = fmaf(pr, y2[k], acc2[g][k]);
+            }
           }
         }
       }
-    }
+      }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
