@@ -53,9 +53,9 @@ TRAFFIC = {
     # kernel: (source hash, bytes per launch, what was captured)
     "prefill_tc": ("ef5cbaad609205d0", 510.16e6 + 118.21e6,
                    "bench.py --part prefill: Llama-2-7B shape S=16384, one launch"),
-    "decode": ("175b125d7157b292", 4.30e9 + 3.57e6,
+    "decode": ("6ccc745edbe73e16", 4.30e9 + 3.63e6,
                "bench.py --part decode: 64 sequences x 32 heads x 4096 slots, one launch"),
-    "decode_fp8": ("175b125d7157b292", 2.15e9 + 3.54e6,
+    "decode_fp8": ("6ccc745edbe73e16", 2.15e9 + 3.55e6,
                    "bench.py --part decode_fp8: the same cache shape in FP8 E4M3, one launch"),
     "rope": ("b80e2ddfaa08bdd0", 134.24e6 + 89.69e6,
              "bench.py --part rope: Q [1, 32, 16384, 128] bf16, one launch"),
