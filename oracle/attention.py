@@ -239,3 +239,54 @@ def backward_head(q, k, v, do, q_pos, k_pos, theta, scale, mask, sink=0, window=
     dq = _rope.rotate(dqr, q_pos, -np.asarray(theta))
     dk = _rope.rotate(dkr, k_pos, -np.asarray(theta))
     return dq, dk, dv
+
+
+def backward_sampled(q, k, v, do, pos, theta, scale, mask, q_rows, k_rows, sink=0, window=0, chunk=512):
+    """The gradients of :func:`backward_head` at selected rows only, for
+    sequences too long for the full S x S matrices: dq at the query rows
+    ``q_rows``, and dk, dv at the key rows ``k_rows``.  It is the same chain
+    rule written per row.  The forward's lse and D = rowsum(dO * O) enter
+    every key row's gradient, so they are computed for all query rows (in
+    chunks of ``chunk`` rows).  Then, with P_mn = exp(scale <Qr_m, Kr_n> -
+    lse_m) on visible pairs and dS_mn = P_mn (<dO_m, V_n> - D_m):
+
+        dq_m = R_m^T scale sum_n dS_mn Kr_n          (row m of dS)
+        dv_n = sum_m P_mn dO_m,  dk_n = R_n^T scale sum_m dS_mn Qr_m   (column n)
+
+    Queries and keys share the positions ``pos`` (self-attention).  Returns
+    (dq [len(q_rows), d], dk [len(k_rows), d], dv [len(k_rows), d]) in
+    float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    pos = np.asarray(pos)
+    neg_theta = -np.asarray(theta)
+    qr = _rope.rotate(q, pos, theta)
+    kr = _rope.rotate(k, pos, theta)
+    S = q.shape[0]
+    lse = np.empty(S)
+    D = np.empty(S)
+    for c0 in range(0, S, chunk):
+        rows = slice(c0, min(S, c0 + chunk))
+        o, l = attention_rows(qr[rows], pos[rows], kr, v, mask, sink, window, scale)
+        lse[rows] = l
+        D[rows] = (o * do[rows]).sum(axis=1)
+
+    def probs(logits, lse_rows, vis):
+        ok = vis & np.isfinite(lse_rows)
+        return np.where(ok, np.exp(np.where(ok, logits - np.where(ok, lse_rows, 0.0), -np.inf)), 0.0)
+
+    qi = np.asarray(q_rows)
+    vis = visible(pos[qi][:, None], pos[None, :], mask, sink, window)
+    p = probs(scale * (qr[qi] @ kr.T), lse[qi][:, None], vis)            # [Rq, S]
+    ds = p * (do[qi] @ v.T - D[qi][:, None])
+    dq = _rope.rotate(scale * (ds @ kr), pos[qi], neg_theta)
+
+    ki = np.asarray(k_rows)
+    vis = visible(pos[:, None], pos[ki][None, :], mask, sink, window)
+    p = probs(scale * (qr @ kr[ki].T), lse[:, None], vis)                # [S, Rk]
+    ds = p * (do @ v[ki].T - D[:, None])
+    dv = p.T @ do
+    dk = _rope.rotate(scale * (ds.T @ qr), pos[ki], neg_theta)
+    return dq, dk, dv

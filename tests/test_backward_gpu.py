@@ -108,3 +108,84 @@ def test_backward_bf16_outputs_and_errors():
     with pytest.raises(api.YarnAttnError) as e:
         api.attn_bwd(api.RopeConfig(kind="plain", head_dim=128), q, q, q, q, q, lse)
     assert e.value.status == 2  # S not a multiple of 128
+
+
+def _heads_per_group(units: int, n_tiles: int) -> int:
+    """Heads per scheduling group of the backward kernels on this GPU (about
+    four waves of CTAs per group), to place checks on both sides of a group
+    boundary."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    return max(1, min(units, (4 * sm + n_tiles - 1) // n_tiles))
+
+
+def test_backward_across_scheduling_groups():
+    """2 x 40 (batch, head) units of 8 tiles each: more units than one
+    scheduling group holds, so later groups' CTAs follow the first group's.
+    O and LSE come from the oracle; the last unit of the first group, the
+    first of the next and both ends are checked."""
+    need_cuda()
+    w = W.Prefill("bwd_groups", 86, 2, 40, 40, 1024, 128, torch.bfloat16, W.RopeSpec("yarn", 1e4, 256, 0, 4.0),
+                  "causal")
+    r = w.rope
+    cfg = api.RopeConfig(kind=r.kind, head_dim=w.d, theta_base=r.theta_base, L_train=r.L_train,
+                         L_target=r.L_target, s=r.s)
+    q, k, v = W.prefill_inputs(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(902)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
+    th, _, ms = R.inv_freq(r.kind, w.d, r.theta_base, r.L_train, r.L_target, r.s)
+    scale = ms * ms / math.sqrt(w.d)
+    pos = np.arange(w.S)
+    qn, kn, vn, gn = f64(q), f64(k), f64(v), f64(dout)
+    o_ref = np.zeros(qn.shape)
+    lse_ref = np.zeros(qn.shape[:3])
+    for b in range(w.B):
+        for h in range(w.Hq):
+            o_ref[b, h], lse_ref[b, h] = A.attention_rows(R.rotate(qn[b, h], pos, th), pos,
+                                                          R.rotate(kn[b, h], pos, th), vn[b, h], w.mask, 0, 0,
+                                                          scale)
+    o_in = torch.from_numpy(o_ref).to("cuda", q.dtype)
+    lse_in = torch.from_numpy(lse_ref).to("cuda", torch.float32).contiguous()
+    dq, dk, dv = api.attn_bwd(cfg, q, k, v, o_in, dout, lse_in, mask=w.mask, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    units = w.B * w.Hq
+    hg = _heads_per_group(units, w.S // 128)
+    assert hg < units, "the case must span more than one scheduling group"
+    for u in sorted({0, hg - 1, hg, units - 1}):
+        b, h = divmod(u, w.Hq)
+        want = A.backward_head(qn[b, h], kn[b, h], vn[b, h], gn[b, h], pos, pos, th, scale, w.mask)
+        for got, ref, n in zip((dq[b, h], dk[b, h], dv[b, h]), want, ("dq", "dk", "dv")):
+            _check(f64(got), ref, f"unit {u} (group {u // hg}) {n}")
+
+
+def test_backward_full_size_sampled_rows():
+    """The backward in the launch configuration the bench times: the
+    Llama-2-7B shape (32 heads, S = 16384, causal, YaRN s = 4), O and LSE
+    from the fused forward as the bench feeds them, several scheduling
+    groups.  Sampled query rows (dq) and key rows (dk, dv) of a head in the
+    first group, the first head of the second and the last head, against
+    the row-sampled float64 oracle, which computes its own forward.  The bar
+    is the one above; it also covers the forward's bf16 O entering
+    D = rowsum(dO * O)."""
+    need_cuda()
+    w = W.LLAMA2_7B
+    r = w.rope
+    cfg = api.RopeConfig(kind=r.kind, head_dim=w.d, theta_base=r.theta_base, L_train=r.L_train,
+                         L_target=r.L_target, s=r.s)
+    q, k, v = W.prefill_inputs(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(901)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
+    o, lse = api.attn_fwd_prefill(cfg, q, k, v, mask=w.mask, return_lse=True)
+    dq, dk, dv = api.attn_bwd(cfg, q, k, v, o, dout, lse, mask=w.mask, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    th, _, ms = R.inv_freq(r.kind, w.d, r.theta_base, r.L_train, r.L_target, r.s)
+    scale = ms * ms / math.sqrt(w.d)
+    pos = np.arange(w.S)
+    hg = _heads_per_group(w.B * w.Hq, w.S // 128)
+    for h in sorted({0, min(hg, w.Hq - 1), w.Hq - 1}):
+        rows_q = W.sample_rows(w.S, 48, h, extra=(4095, 4096, 8191)).numpy()
+        rows_k = W.sample_rows(w.S, 48, 100 + h, extra=(4095, 4096, 16256)).numpy()
+        sq, sk, sv = A.backward_sampled(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), f64(dout[0, h]), pos, th, scale,
+                                        w.mask, rows_q, rows_k)
+        _check(f64(dq[0, h, rows_q]), sq, f"head {h} dq rows")
+        _check(f64(dk[0, h, rows_k]), sk, f"head {h} dk rows")
+        _check(f64(dv[0, h, rows_k]), sv, f"head {h} dv rows")

@@ -336,3 +336,23 @@ def test_backward_rows_and_blocks_are_consistent():
     _, _, dv_a = A.backward_head(q[:5], k, v, g[:5], pos[:5], pos, theta, 0.5, "causal")
     _, _, dv_b = A.backward_head(q[5:], k, v, g[5:], pos[5:], pos, theta, 0.5, "causal")
     np.testing.assert_allclose(dv, dv_a + dv_b, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask,sink,window", [("causal", 0, 0), ("sink_window", 2, 9), ("none", 0, 0)])
+def test_backward_sampled_rows_match_the_full_backward(mask, sink, window):
+    """The row-sampled backward (used where S x S matrices do not fit) gives
+    the rows of the full backward, which finite differences pin above; the
+    sampled rows include the first, the last and rows split across its
+    lse / D chunks."""
+    rng = np.random.default_rng(33)
+    S, d = 40, 8
+    q, k, v, g = rng.standard_normal((4, S, d))
+    theta = rope.base_frequencies(d, 1e4) / 2.0
+    pos = np.arange(S)
+    dq, dk, dv = A.backward_head(q, k, v, g, pos, pos, theta, 0.7, mask, sink, window)
+    rows_q = np.array([0, 5, 16, 17, 39])
+    rows_k = np.array([0, 1, 15, 30, 39])
+    sq, sk, sv = A.backward_sampled(q, k, v, g, pos, theta, 0.7, mask, rows_q, rows_k, sink, window, chunk=16)
+    np.testing.assert_allclose(sq, dq[rows_q], atol=1e-12, rtol=1e-10)
+    np.testing.assert_allclose(sk, dk[rows_k], atol=1e-12, rtol=1e-10)
+    np.testing.assert_allclose(sv, dv[rows_k], atol=1e-12, rtol=1e-10)
