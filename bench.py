@@ -287,6 +287,81 @@ def time_prefill_workload(w, dev, stream, reps: int = 3):
             "ring_blocks": w.ring_blocks, "mask": w.mask}
 
 
+def time_ring_blocks(w, dev, stream, reps: int = 2):
+    """The ring workload computed as each device of a multi-GPU ring would:
+    Q and K rotated once (each device rotates its own blocks), then query
+    block I takes KV blocks I, I-1, ..., 0, one attn_fwd_prefill_kv_block
+    call each on the rotated operands into a float32 partial, merged by
+    attn_merge_partial (the last merge writes the bf16 output).  Device
+    time of the rotation and all blocks' calls, with the merge kernel's
+    share and bandwidth; no communication is included."""
+    cfg_rot = cfg_of(w)
+    _, _, mscale = api.yarn_inv_freq(cfg_rot)
+    cfg = api.RopeConfig(kind="none", head_dim=w.d)
+    scale = mscale * mscale / math.sqrt(w.d)
+    q0, k0, v = W.prefill_inputs(w, dev)
+    q, k = torch.empty_like(q0), torch.empty_like(k0)
+    N = w.ring_blocks
+    bs = w.S // N
+    final = torch.empty_like(q)
+    acc = torch.empty(w.B, w.Hq, bs, w.d, dtype=torch.float32, device=dev)
+    part = torch.empty_like(acc)
+    lacc = torch.empty(w.B, w.Hq, bs, dtype=torch.float32, device=dev)
+    lpart = torch.empty_like(lacc)
+    ws = torch.empty(max(1, api.prefill_kv_block_workspace_bytes(cfg, q.dtype, w.B, w.Hq, w.Hkv, bs, bs, w.d)),
+                     dtype=torch.uint8, device=dev)
+    merges = []
+
+    def ring(record=False):
+        api.rope_apply(cfg_rot, q0, out=q, stream=stream)
+        api.rope_apply(cfg_rot, k0, out=k, stream=stream)
+        for I in range(N):
+            rows = slice(I * bs, (I + 1) * bs)
+            qi = q[:, :, rows]
+            order = list(range(I, -1, -1))  # I, I-1, ..., 0: the causal ring skips blocks after I
+            for step, j in enumerate(order):
+                keys = slice(j * bs, (j + 1) * bs)
+                last = step == len(order) - 1
+                if step == 0:
+                    api.attn_fwd_prefill_kv_block(cfg, qi, k[:, :, keys], v[:, :, keys], I * bs, j * bs,
+                                                  mask=w.mask, softmax_scale=scale,
+                                                  out=final[:, :, rows] if last else acc, lse=lacc,
+                                                  workspace=ws, stream=stream)
+                    continue
+                api.attn_fwd_prefill_kv_block(cfg, qi, k[:, :, keys], v[:, :, keys], I * bs, j * bs, mask=w.mask,
+                                              softmax_scale=scale, out=part, lse=lpart, workspace=ws,
+                                              stream=stream)
+                if record:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                api.attn_merge_partial(acc, lacc, part, lpart, out=final[:, :, rows] if last else None,
+                                       stream=stream)
+                if record:
+                    b.record(stream)
+                    merges.append((a, b, last))
+
+    ring()
+    torch.cuda.synchronize()
+    ms = statistics.median(timed(ring, reps, stream))
+    ring(record=True)
+    torch.cuda.synchronize()
+    api.sync_status()
+    fused = api.attn_fwd_prefill(cfg_rot, q0, k0, v, mask=w.mask, ring_blocks=N)
+    diff = (fused.float() - final.float()).abs().max().item()
+    del fused
+    merge_ms = sum(a.elapsed_time(b) for a, b, _ in merges)
+    # per merge: O_acc read + written, O_part read (float32), four lse vectors; the last one per query block
+    # also writes the bf16 output
+    per = w.B * w.Hq * bs
+    merge_bytes = sum(per * w.d * 4 * 3 + per * 4 * 4 + (per * w.d * 2 if last else 0) for _, _, last in merges)
+    flops = prefill_flops(w)
+    del q0, k0, q, k, v, final, acc, part, lacc, lpart, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.name + "_one_kv_block_per_call", "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+            "kv_block_calls": N * (N + 1) // 2, "merges": len(merges), "merge_ms_total": merge_ms,
+            "merge_GB/s": merge_bytes / (merge_ms * 1e-3) / 1e9, "max_abs_diff_vs_fused_call": diff}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -476,6 +551,11 @@ def run_ours(args):
             r = time_prefill_workload(wo, dev, stream)
             r["frac_of_burst"] = r["TFLOP/s"] / tf_burst
             others.append(r)
+    ring_blocks = None
+    if not args.no_other_workloads:
+        ring_blocks = time_ring_blocks(W.RING_128K, dev, stream)
+        ring_blocks["frac_of_burst"] = ring_blocks["TFLOP/s"] / tf_burst
+        ring_blocks["merge_frac_of_hbm"] = ring_blocks["merge_GB/s"] / hbm
 
     if rank != 0:
         if dist:
@@ -511,6 +591,7 @@ def run_ours(args):
                                     "frac": dec8_gbs / hbm, "traffic": traffic("decode_fp8")}},
         "backward": bwd,
         "other_prefill_workloads": others,
+        "ring_building_blocks": ring_blocks,
         "rope_apply": {"workload": "Q and K of " + w.name, "value": rope_gbs, "unit": "GB/s",
                        "ms": rope_ms,
                        "roofline": {"bound": "hbm", "achieved": rope_gbs, "peak": hbm, "unit": "GB/s",

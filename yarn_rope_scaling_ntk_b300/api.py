@@ -189,6 +189,12 @@ def prefill_workspace_bytes(cfg: RopeConfig, dtype: torch.dtype, B, Hq, Hkv, S, 
     return int(load_library().yr_prefill_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, S, d))
 
 
+def prefill_kv_block_workspace_bytes(cfg: RopeConfig, dtype: torch.dtype, B, Hq, Hkv, Sq, Skv, d) -> int:
+    c = cfg.c()
+    code = F32 if dtype == torch.float32 else BF16
+    return int(load_library().yr_prefill_kv_block_workspace_bytes(ctypes.byref(c), code, B, Hq, Hkv, Sq, Skv, d))
+
+
 def attn_fwd_prefill(cfg: RopeConfig, q, k, v, mask: str = "causal", sink: int = 0,
                      window: int = 0, ring_blocks: int = 1, softmax_scale: float = 0.0,
                      out=None, lse=None, return_lse: bool = False, workspace=None, stream=None):

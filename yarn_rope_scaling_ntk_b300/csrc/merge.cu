@@ -7,13 +7,15 @@
 // softmax; "Context Window Scaling ...", Section 5).
 //
 // Memory-bound: one warp per row; each lane owns 4 consecutive float32
-// elements (16-byte loads and stores).
+// elements of each 128-element chunk (16-byte loads and stores).
 #include "common.cuh"
 #include "internal.h"
 
 namespace yr {
 namespace {
 
+// CH = chunks of 128 floats per row (d <= 128 CH).
+template <int CH>
 __global__ void __launch_bounds__(256) merge_kernel(MergeLaunch a) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)a.B * a.H * a.S;
@@ -22,6 +24,22 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeLaunch a) {
   const int s = (int)(row % a.S);
   const int64_t bh = row / a.S;
   const int h = (int)(bh % a.H), b = (int)(bh / a.H);
+  float* oa = a.o_acc + b * a.as[0] + h * a.as[1] + (int64_t)s * a.as[2];
+  const float* op = a.o_part + b * a.ps[0] + h * a.ps[1] + (int64_t)s * a.ps[2];
+  // Both rows are loaded together with the lse values (no dependent second
+  // round trip); a side with weight 0 (an empty partial, lse = -inf) is
+  // dropped by a select, never multiplied, so an accumulator that holds
+  // nothing yet may contain anything.
+  constexpr int kMaxChunks = CH;
+  float4 xa[kMaxChunks], xp[kMaxChunks];
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int c = lane * 4 + i * 128;
+    if (c < a.d) {
+      xa[i] = *reinterpret_cast<const float4*>(oa + c);
+      xp[i] = *reinterpret_cast<const float4*>(op + c);
+    }
+  }
   const float la = a.lse_acc[row], lp = a.lse_part[row];
   const float mx = fmaxf(la, lp);
   float wa = 0.f, wp = 0.f, lnew = -INFINITY;
@@ -32,20 +50,16 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeLaunch a) {
     wp = ep / tot;
     lnew = mx + logf(tot);
   }
-  float* oa = a.o_acc + b * a.as[0] + h * a.as[1] + (int64_t)s * a.as[2];
-  const float* op = a.o_part + b * a.ps[0] + h * a.ps[1] + (int64_t)s * a.ps[2];
-  for (int c = lane * 4; c < a.d; c += 128) {
-    // a side with weight 0 (an empty partial, lse = -inf) is not read, so an
-    // accumulator that holds nothing yet may contain anything
-    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (wa != 0.f) {
-      const float4 x = *reinterpret_cast<const float4*>(oa + c);
-      z = make_float4(wa * x.x, wa * x.y, wa * x.z, wa * x.w);
-    }
-    if (wp != 0.f) {
-      const float4 y = *reinterpret_cast<const float4*>(op + c);
-      z = make_float4(z.x + wp * y.x, z.y + wp * y.y, z.z + wp * y.z, z.w + wp * y.w);
-    }
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int c = lane * 4 + i * 128;
+    if (c >= a.d) continue;
+    const float4 x = xa[i], y = xp[i];
+    float4 z;
+    z.x = (wa != 0.f ? wa * x.x : 0.f) + (wp != 0.f ? wp * y.x : 0.f);
+    z.y = (wa != 0.f ? wa * x.y : 0.f) + (wp != 0.f ? wp * y.y : 0.f);
+    z.z = (wa != 0.f ? wa * x.z : 0.f) + (wp != 0.f ? wp * y.z : 0.f);
+    z.w = (wa != 0.f ? wa * x.w : 0.f) + (wp != 0.f ? wp * y.w : 0.f);
     *reinterpret_cast<float4*>(oa + c) = z;
     if (a.o_final) {
       const int64_t off = b * a.fs[0] + h * a.fs[1] + (int64_t)s * a.fs[2] + c;
@@ -94,7 +108,12 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;  // 8 warps (rows) per CTA
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  merge_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  const int ch = (a.d + 127) / 128;
+  if (ch <= 1) merge_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else if (ch <= 2) merge_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else if (ch <= 4) merge_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else if (ch <= 8) merge_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
