@@ -209,8 +209,9 @@ yr_status attn_fwd_prefill_kv_block(const yr_rope_cfg* cfg, const void* q, const
  * disjoint key sets and normalised over their own keys:
  *   L = ln(e^La + e^Lp),  O = e^(La - L) Oa + e^(Lp - L) Op
  * ("Context Length Extension", Ring Attention: partial results are combined
- * using online softmax).  A side whose lse is -inf is empty and is not read
- * (so a fresh accumulator needs only lse_acc = -inf).
+ * using online softmax).  A side whose lse is -inf is empty: its O is
+ * loaded but dropped, never multiplied, so a fresh accumulator needs only
+ * lse_acc = -inf (its O buffer must exist; its contents do not matter).
  * o_acc    : device float32 [B, H, S, d] (strides acc_strides), updated.
  * lse_acc  : device float32 [B, H, S] contiguous, updated.
  * o_part, lse_part : the partial, same shapes (o strides part_strides).

@@ -75,7 +75,7 @@ struct DecodeLaunch {
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
 struct PrefillLaunch {
-  const void* q;  // bf16 rotated (or raw when rotate_q_in_kernel)
+  const void* q;  // bf16, rotated
   const void* k;  // bf16 rotated
   const void* v;  // bf16
   void* o;
