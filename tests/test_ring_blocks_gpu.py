@@ -140,3 +140,55 @@ def test_empty_kv_block_gives_empty_rows():
     o, lse = api.attn_fwd_prefill_kv_block(_cfg(64), q, k, k, 10, 0)
     torch.cuda.synchronize()
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_ring_blocks_full_size_sampled_rows():
+    """The ring 128K workload in the launch configuration the bench times
+    for the building blocks: Q and K rotated once by rope_apply, then query
+    block I takes KV blocks I, I-1, ..., 0 of the rotated operands (kind
+    "none", the YaRN softmax scale passed explicitly), one
+    attn_fwd_prefill_kv_block call each into float32 partials merged by
+    attn_merge_partial, the last merge writing bf16.  Sampled rows of three
+    heads, with the block edges, against the float64 oracle."""
+    need_cuda()
+    w = W.RING_128K
+    r = w.rope
+    cfg_rot = api.RopeConfig(kind=r.kind, head_dim=w.d, theta_base=r.theta_base, L_train=r.L_train,
+                             L_target=r.L_target, s=r.s)
+    _, _, mscale = api.yarn_inv_freq(cfg_rot)
+    cfg = api.RopeConfig(kind="none", head_dim=w.d)
+    scale = mscale * mscale / math.sqrt(w.d)
+    q0, k0, v = W.prefill_inputs(w, "cuda")
+    q, k = api.rope_apply(cfg_rot, q0), api.rope_apply(cfg_rot, k0)
+    N, bs = w.ring_blocks, w.S // w.ring_blocks
+    final = torch.empty_like(q0)
+    acc = torch.empty(w.B, w.Hq, bs, w.d, dtype=torch.float32, device="cuda")
+    part, lacc, lpart = torch.empty_like(acc), acc.new_empty(w.B, w.Hq, bs), acc.new_empty(w.B, w.Hq, bs)
+    for I in range(N):
+        rows = slice(I * bs, (I + 1) * bs)
+        for step, j in enumerate(range(I, -1, -1)):
+            keys = slice(j * bs, (j + 1) * bs)
+            last = j == 0
+            if step == 0:
+                api.attn_fwd_prefill_kv_block(cfg, q[:, :, rows], k[:, :, keys], v[:, :, keys], I * bs, j * bs,
+                                              softmax_scale=scale, out=final[:, :, rows] if last else acc,
+                                              lse=lacc)
+                continue
+            api.attn_fwd_prefill_kv_block(cfg, q[:, :, rows], k[:, :, keys], v[:, :, keys], I * bs, j * bs,
+                                          softmax_scale=scale, out=part, lse=lpart)
+            api.attn_merge_partial(acc, lacc, part, lpart, out=final[:, :, rows] if last else None)
+    torch.cuda.synchronize()
+    api.sync_status()
+    th, _, ms = R.inv_freq(r.kind, w.d, r.theta_base, r.L_train, r.L_target, r.s)
+    oscale = ms * ms / math.sqrt(w.d)
+    pos = np.arange(w.S)
+    edges = tuple(x for I in range(1, N) for x in (I * bs - 1, I * bs))
+    got, want = [], []
+    for h in (0, 13, 31):
+        rws = W.sample_rows(w.S, 24, 200 + h, extra=edges).numpy()
+        kr = R.rotate(f64(k0[0, h]), pos, th)
+        qr = R.rotate(f64(q0[0, h, rws]), rws, th)
+        o, _ = A.attention_rows(qr, rws, kr, f64(v[0, h]), w.mask, 0, 0, oscale)
+        got.append(f64(final[0, h, rws]))
+        want.append(o)
+    assert_attn_close(np.concatenate(got), np.concatenate(want), "ring blocks 128K")
