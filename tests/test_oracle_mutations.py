@@ -108,3 +108,81 @@ def test_reversed_yarn_blend_is_caught(monkeypatch):
 def test_ring_slot_misindex_is_caught(monkeypatch):
     monkeypatch.setattr(A, "decode_logical_to_physical", _decode_ring_misindexed)
     assert _fails(TA.test_decode_against_streaming_simulation, 23, 4, 6)
+
+
+# --- the backward, the merge of partials and FP8 decoding -------------------
+
+import oracle.quant as Q  # noqa: E402
+from tests import test_oracle_quant as TQ  # noqa: E402
+
+
+def _backward_without_inverse_rotation(q, k, v, do, q_pos, k_pos, theta, scale, mask, sink=0, window=0):
+    # forgets R^T: the gradients of the rotated q and k are returned as they are
+    dq, dk, dv = A.__dict__["_orig_backward"](q, k, v, do, q_pos, k_pos, theta, scale, mask, sink, window)
+    return R.rotate(dq, q_pos, theta), R.rotate(dk, k_pos, theta), dv
+
+
+def _backward_without_scale(q, k, v, do, q_pos, k_pos, theta, scale, mask, sink=0, window=0):
+    # forgets the softmax scale in dq and dk
+    dq, dk, dv = A.__dict__["_orig_backward"](q, k, v, do, q_pos, k_pos, theta, scale, mask, sink, window)
+    return dq / scale, dk / scale, dv
+
+
+def _backward_without_rowsum_term(q, k, v, do, q_pos, k_pos, theta, scale, mask, sink=0, window=0):
+    # dS = P * dP, the D = rowsum(dO * O) term dropped
+    qr, kr = R.rotate(np.asarray(q, float), q_pos, theta), R.rotate(np.asarray(k, float), k_pos, theta)
+    logits = np.where(A.visible(np.asarray(q_pos)[:, None], np.asarray(k_pos)[None, :], mask, sink, window),
+                      scale * (qr @ kr.T), -np.inf)
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    ds = p * (np.asarray(do, float) @ np.asarray(v, float).T)
+    dq = R.rotate(scale * (ds @ kr), q_pos, -np.asarray(theta))
+    dk = R.rotate(scale * (ds.T @ qr), k_pos, -np.asarray(theta))
+    return dq, dk, p.T @ np.asarray(do, float)
+
+
+def _merge_weights_swapped(parts):
+    # two partials, each weighted by the other's share of the total
+    (oa, la), (ob, _) = parts
+    _, lse = A.__dict__["_orig_merge"](parts)
+    with np.errstate(invalid="ignore"):
+        wa = np.nan_to_num(np.exp(np.asarray(la) - lse))[:, None]
+    return (1 - wa) * np.asarray(oa) + wa * np.asarray(ob), lse
+
+
+def _e4m3_bias_8(codes):
+    # exponent bias 8 instead of 7: every value halved
+    return Q.__dict__["_orig_e4m3"](codes) / 2.0
+
+
+@pytest.fixture(autouse=True)
+def _keep_more_originals():
+    A._orig_backward = A.backward_head
+    A._orig_merge = A.merge_partials
+    Q._orig_e4m3 = Q.e4m3_to_float
+    yield
+
+
+def test_backward_missing_inverse_rotation_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "backward_head", _backward_without_inverse_rotation)
+    assert _fails(TA.test_backward_matches_finite_differences, "causal", 0, 0)
+
+
+def test_backward_missing_scale_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "backward_head", _backward_without_scale)
+    assert _fails(TA.test_backward_matches_finite_differences, "causal", 0, 0)
+
+
+def test_backward_dropped_rowsum_term_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "backward_head", _backward_without_rowsum_term)
+    assert _fails(TA.test_backward_matches_finite_differences, "none", 0, 0)
+
+
+def test_merge_with_swapped_weights_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "merge_partials", _merge_weights_swapped)
+    assert _fails(TA.test_merge_partials_lse_is_logsumexp_and_empty_rows)
+
+
+def test_e4m3_wrong_exponent_bias_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "e4m3_to_float", _e4m3_bias_8)
+    assert _fails(TQ.test_e4m3_all_codes_match_torch)
