@@ -2,6 +2,7 @@
 oracle (on the CPU, through monkeypatch) and checks that a pin test fails."""
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -186,3 +187,44 @@ def test_merge_with_swapped_weights_is_caught(monkeypatch):
 def test_e4m3_wrong_exponent_bias_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "e4m3_to_float", _e4m3_bias_8)
     assert _fails(TQ.test_e4m3_all_codes_match_torch)
+
+
+# --- the YaRN ramp interior and the base frequencies, against hand values ---
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _ramp_denominator_beta(r, alpha, beta):
+    # (r - alpha) / beta instead of (r - alpha) / (beta - alpha)
+    return np.clip((np.asarray(r, dtype=np.float64) - alpha) / beta, 0.0, 1.0)
+
+
+def _yarn_blend_divides(kind, d, b, L_train=0.0, L_target=0.0, s=0.0, alpha=1.0, beta=32.0, dim_scale=None):
+    # the blend read as theta / ((1 - gamma) s + gamma): the factor blended, not the frequency
+    th, cls, ms = R.__dict__["_orig_inv_freq"](kind, d, b, L_train, L_target, s, alpha, beta, dim_scale)
+    if kind == "yarn":
+        s_ = R.resolve_scale(L_train, L_target, s)
+        g = R.ramp_gamma(float(L_train) / R.wavelength(d, b), alpha, beta)
+        th = R.base_frequencies(d, b) / ((1 - g) * s_ + g)
+    return th, cls, ms
+
+
+def _base_exponent_i_over_d(d, b):
+    # b^(-i/d) instead of b^(-2i/d)
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.power(float(b), -i / d)
+
+
+def test_ramp_denominator_is_caught_by_hand_values(monkeypatch):
+    monkeypatch.setattr(R, "ramp_gamma", _ramp_denominator_beta)
+    assert _fails(TR.test_yarn_ramp_hand_values, GOLDEN)
+
+
+def test_blend_of_the_factor_is_caught_by_hand_values(monkeypatch):
+    monkeypatch.setattr(R, "inv_freq", _yarn_blend_divides)
+    assert _fails(TR.test_yarn_ramp_hand_values, GOLDEN)
+
+
+def test_base_exponent_is_caught_by_hand_values(monkeypatch):
+    monkeypatch.setattr(R, "base_frequencies", _base_exponent_i_over_d)
+    assert _fails(TR.test_ntk_exercise2_and_base_frequencies_hand_values, GOLDEN)

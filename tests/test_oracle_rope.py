@@ -238,3 +238,42 @@ def test_perdim_rejects_bad_vectors():
     for bad in (None, np.ones(3), np.array([1.0] * 31 + [0.0]), np.array([1.0] * 31 + [np.nan])):
         with pytest.raises((ValueError, TypeError)):
             rope.inv_freq("perdim", 64, 1e4, 64, dim_scale=bad)
+
+
+def test_yarn_ramp_hand_values(golden_dir):
+    """The ramp's interior against values worked by hand from the page's
+    definitions (wavelength, ratio to the training window, linear ramp,
+    frequency blend): every field of every row, so a wrong denominator, a
+    wrong blend or a wrong exponent changes at least one of them."""
+    g = json.load(open(os.path.join(golden_dir, "yarn_ramp_hand.json")))
+    for case in g["cases"]:
+        d, b, L, s = case["d"], case["theta_base"], case["L_train"], case["s"]
+        th_p, cls, _ = rope.inv_freq("yarn", d, b, L, 0, s)
+        base = rope.base_frequencies(d, b)
+        lam = rope.wavelength(d, b)
+        for row in case["rows"]:
+            i = row["i"]
+            assert base[i] == pytest.approx(row["theta"], rel=1e-13)
+            assert lam[i] == pytest.approx(row["lambda"], rel=1e-13)
+            assert L / lam[i] == pytest.approx(row["r"], rel=1e-13)
+            gam = float(rope.ramp_gamma(L / lam[i], 1.0, 32.0))
+            assert gam == pytest.approx(row["gamma"], rel=1e-12, abs=1e-15)
+            assert th_p[i] == pytest.approx(row["theta_prime"], rel=1e-13)
+            assert int(cls[i]) == row["class"]
+
+
+def test_ntk_exercise2_and_base_frequencies_hand_values(golden_dir):
+    """Exercise 2 of the NTK section (4K -> 32K, d = 128) under the adopted
+    reading, and the plain frequencies b^(-2i/d) at interior i, against values
+    worked by hand."""
+    g = json.load(open(os.path.join(golden_dir, "ntk_exercise2_hand.json")))
+    d, b = g["d"], g["theta_base"]
+    s = rope.resolve_scale(g["L_train"], g["L_target"], 0.0)
+    assert s == g["s"]
+    assert rope.ntk_base(b, s, d) == pytest.approx(g["ntk_base"], rel=1e-14)
+    th, _, _ = rope.inv_freq("ntk", d, b, g["L_train"], g["L_target"])
+    for i, want in g["ntk_theta"].items():
+        assert th[int(i)] == pytest.approx(want, rel=1e-13)
+    base = rope.base_frequencies(d, b)
+    for i, want in g["plain_theta"].items():
+        assert base[int(i)] == pytest.approx(want, rel=1e-14)
