@@ -166,7 +166,9 @@ size_t yr_prefill_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int3
  * *_strides : host int64[3] (batch, head, position), in elements.
  * d ∈ {64, 128}.  S >= 1 (a ragged last tile is masked).
  * workspace : device scratch of yr_prefill_workspace_bytes(); holds the
- *       rotated bfloat16 copy of K (and of Q and V for float32 inputs).
+ *       rotated bfloat16 copies of Q and K (when kind is not NONE, or the
+ *       inputs are float32) and the bfloat16 copy of V (float32 inputs
+ *       only); kind NONE with bfloat16 inputs needs none.
  * The matrix products run on bfloat16 operands with float32 accumulation. */
 yr_status attn_fwd_prefill(const yr_rope_cfg* cfg, const void* q, const void* k, const void* v,
                            void* o, float* lse, int32_t in_dtype,
@@ -332,6 +334,12 @@ yr_status attn_fwd_decode_sinkwindow_noalloc(const yr_rope_cfg* cfg, const void*
  * bounded waits set; returns YR_ERR_TIMEOUT if one gave up, YR_ERR_CUDA on a
  * CUDA error, YR_OK otherwise. */
 yr_status yr_sync_status(void* stream);
+
+/* Number of kernels the library has launched in this process so far, over
+ * every entry point and device (each successful launch counts once).  Host
+ * only; for counting the launches inside a timed region.  Not part of the
+ * method: the pages have no counterpart. */
+uint64_t yr_kernel_launch_count(void);
 
 /* Thread-local text of the last error (empty when none). */
 const char* yr_last_error_message(void);

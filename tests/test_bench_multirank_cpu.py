@@ -51,3 +51,32 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.reduce_max(3.5) == 3.5
     assert bench.whole_job_rate(1.0, 4, 1, 2.0) == pytest.approx(2000.0)
+
+
+def _bench_lines(*args, env=None):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_bench_gpus_n_starts_n_ranks_itself(n):
+    """``bench.py --gpus N`` with no launcher environment starts N rank
+    processes that form one group; rank 0 alone prints one line for the job."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    lines = _bench_lines("--gpus", str(n), "--steps", "2", "--launcher-check", env=env)
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == n and lines[0]["ranks_joined"] == n
+
+
+def test_bench_under_a_launcher_does_not_start_ranks_again():
+    """Under torchrun (WORLD_SIZE set) each process is one rank already: a
+    single-rank environment runs one process and prints one line."""
+    env = dict(os.environ, RANK="0", LOCAL_RANK="0", WORLD_SIZE="1")
+    lines = _bench_lines("--gpus", "2", "--steps", "2", "--launcher-check", env=env)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 1

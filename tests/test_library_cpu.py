@@ -161,3 +161,51 @@ def test_perdim_inv_freq_matches_oracle_and_rejects_bad_vectors(lib):
         with pytest.raises(api.YarnAttnError) as e:
             api.yarn_inv_freq(api.RopeConfig(kind="perdim", head_dim=128, L_train=4096, dim_scale=bad))
         assert e.value.status == 1
+
+
+def test_noalloc_reports_argument_errors_before_its_size_limit(lib):
+    """The allocation-free decode entry reports the same argument errors as
+    the workspace entry, even when the split count it is given would also
+    exceed its fixed scratch array; no pointer is touched."""
+    cfg = api.RopeConfig(kind="plain", head_dim=128).c()
+    args = lambda B, Hq, Hkv, d, splits: (ctypes.byref(cfg), None, None, None, None, None, B, Hq, Hkv, d, 4,
+                                          4092, None, None, splits, None)
+    # Hq % Hkv != 0 with 4000 splits (far above the array): the shape error wins
+    assert lib.attn_fwd_decode_sinkwindow_noalloc(*args(64, 30, 8, 128, 4000)) == 1
+    assert b"Hq % Hkv" in lib.yr_last_error_message()
+    # unsupported head dimension
+    assert lib.attn_fwd_decode_sinkwindow_noalloc(*args(64, 32, 32, 96, 4000)) == 2
+    assert b"head dimension" in lib.yr_last_error_message()
+    # num_splits above the entry points' limit
+    assert lib.attn_fwd_decode_sinkwindow_noalloc(*args(64, 32, 32, 128, 5000)) == 1
+    assert b"num_splits" in lib.yr_last_error_message()
+    # a valid shape whose split scratch exceeds the array
+    assert lib.attn_fwd_decode_sinkwindow_noalloc(*args(64, 32, 32, 128, 64)) == 1
+    assert b"scratch" in lib.yr_last_error_message()
+
+
+def test_noalloc_python_wrapper_validates_like_its_sibling(lib):
+    """The Python wrapper of the allocation-free entry checks shapes, dtypes
+    and layouts before it calls the library (CPU tensors: the shape errors
+    come before the device check)."""
+    cfg = api.RopeConfig(kind="plain", head_dim=128)
+    B, H, d, sink, win = 2, 4, 128, 4, 60
+    q = torch.zeros(B, H, d, dtype=torch.bfloat16)
+    kc = torch.zeros(B, H, sink + win, d, dtype=torch.bfloat16)
+    nv = torch.full((B,), sink + win, dtype=torch.int32)
+    rs = torch.zeros(B, dtype=torch.int32)
+    bad = [
+        dict(k_cache=kc[:, :, :-1].contiguous()),              # cache shorter than sink + window
+        dict(q=q.float()),                                       # float32 query
+        dict(v_cache=kc.transpose(2, 3).contiguous().transpose(2, 3)),  # not contiguous
+        dict(n_valid=nv.long()),                                 # int64 counts
+        dict(out=torch.zeros(B, H, d, dtype=torch.float32)),     # wrong output dtype
+        dict(lse=torch.zeros(B, H + 1, dtype=torch.float32)),    # wrong lse shape
+        dict(),                                                  # CPU tensors
+    ]
+    for change in bad:
+        a = dict(q=q, k_cache=kc, v_cache=kc, n_valid=nv, ring_start=rs, out=None, lse=None)
+        a.update(change)
+        with pytest.raises(ValueError):
+            api.attn_fwd_decode_sinkwindow_noalloc(cfg, a["q"], a["k_cache"], a["v_cache"], a["n_valid"],
+                                                   a["ring_start"], sink, win, out=a["out"], lse=a["lse"])

@@ -123,7 +123,8 @@ def test_llama2_7b_shape_sampled_rows():
     need_cuda()
     w = W.LLAMA2_7B
     q, k, v = W.prefill_inputs(w, "cuda")
-    check(w, q, k, v, 32, extra_rows=(4095, 4096, 8191, 8192))
+    # 256 seeded query rows per head on all 32 heads, plus tile and block edges
+    check(w, q, k, v, w.rows_per_head, extra_rows=(4095, 4096, 8191, 8192))
 
 
 def test_ring_128k_sampled_rows():
@@ -132,14 +133,16 @@ def test_ring_128k_sampled_rows():
     q, k, v = W.prefill_inputs(w, "cuda")
     bs = w.S // w.ring_blocks
     edges = tuple(x for j in range(1, w.ring_blocks) for x in (j * bs - 1, j * bs, j * bs + 1))
-    check(w, q, k, v, 8, extra_rows=edges)
+    # 128 seeded query rows per head on all 32 heads, plus every ring-block edge
+    check(w, q, k, v, w.rows_per_head, extra_rows=edges)
 
 
 @pytest.mark.parametrize("wl", [W.LLAMA3_8B_GQA, W.LLAMA3_8B_GQA_SW])
 def test_llama3_8b_gqa_sampled_rows(wl):
     need_cuda()
     q, k, v = W.prefill_inputs(wl, "cuda")
-    check(wl, q, k, v, 4, extra_rows=(8191, 8192, 8193, 8194, 8195, 8196, 8197, 16384))
+    # 32 seeded query rows per (sequence, head): 4096 rows per mask, plus the window edges
+    check(wl, q, k, v, wl.rows_per_head, extra_rows=(8191, 8192, 8193, 8194, 8195, 8196, 8197, 16384))
 
 
 def test_perdim_scale_vector_prefill_all_rows():

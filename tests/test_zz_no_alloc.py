@@ -65,3 +65,20 @@ def test_noalloc_rejects_scratch_above_its_limit():
     # 64 splits x 64 x 32 x 130 x 4 bytes is far above the fixed array
     st, _, _ = _call_noalloc(lib, cfg, w, inp, 64)
     assert st == 1 and b"scratch" in lib.yr_last_error_message()
+
+
+def test_noalloc_python_wrapper_on_the_gpu():
+    """The Python wrapper of the allocation-free entry, with caller-owned
+    outputs, against the workspace entry (a split count that needs scratch)."""
+    need_cuda()
+    cfg = api.RopeConfig(kind="plain", head_dim=128)
+    w, inp = _inputs(74, 2, 8, 4, 4, 700)
+    q, kc, vc, nv, rs = inp
+    want_o, want_l = api.attn_fwd_decode_sinkwindow(cfg, q, kc, vc, nv, rs, w.sink, w.window, num_splits=3,
+                                                    return_lse=True)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, dtype=torch.float32, device="cuda")
+    api.attn_fwd_decode_sinkwindow_noalloc(cfg, q, kc, vc, nv, rs, w.sink, w.window, num_splits=3, out=o, lse=lse)
+    api.sync_status()
+    assert_attn_close(f64(o), f64(want_o), "noalloc wrapper vs workspace entry")
+    np.testing.assert_allclose(f64(lse), f64(want_l), atol=1e-2)

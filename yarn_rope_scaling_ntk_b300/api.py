@@ -115,6 +115,7 @@ def load_library():
         "attn_fwd_decode_sinkwindow_noalloc": (I32, [cfgp, _P, _P, _P, _P, _P, I32, I32, I32, I32,
                                                      I32, I32, _P, _P, I32, _P]),
         "yr_sync_status": (I32, [_P]),
+        "yr_kernel_launch_count": (ctypes.c_uint64, []),
         "yr_last_error_message": (ctypes.c_char_p, []),
         "yr_version": (ctypes.c_char_p, []),
     }
@@ -310,16 +311,12 @@ def attn_bwd(cfg: RopeConfig, q, k, v, o, dout, lse, mask: str = "causal", sink:
     return dq, dk, dv
 
 
-def decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits=0) -> int:
-    return int(load_library().yr_decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits))
-
-
-def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ring_start,
-                               sink: int, window: int, num_splits: int = 0, out=None, lse=None,
-                               return_lse: bool = False, workspace=None, stream=None):
-    """q [B, Hq, d] bf16; caches [B, Hkv, sink + window, d] bf16 (contiguous);
-    n_valid / ring_start int32 [B].  Returns o [B, Hq, d] (and lse [B, Hq])."""
-    lib = load_library()
+def _check_decode_args(q, k_cache, v_cache, n_valid, ring_start, sink, window, out=None, lse=None):
+    """Shapes, dtypes and layouts of a bfloat16-cache decode call (the kernel
+    indexes the caches as contiguous [B, Hkv, sink + window, d]); returns
+    (B, Hq, d, Hkv)."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and the caches [B, Hkv, sink + window, d]")
     B, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     for t in (q, k_cache, v_cache):
@@ -330,6 +327,27 @@ def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ri
     for t in (n_valid, ring_start):
         if t.dtype != torch.int32 or t.shape != (B,):
             raise ValueError("n_valid and ring_start must be int32 [B]")
+    if out is not None and (out.dtype != torch.bfloat16 or out.shape != (B, Hq, d) or not out.is_contiguous()):
+        raise ValueError("out must be contiguous bfloat16 [B, Hq, d]")
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, Hq) or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous float32 [B, Hq]")
+    devs = {t.device for t in (q, k_cache, v_cache, n_valid, ring_start, out, lse) if t is not None}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError("every tensor must be on the same CUDA device")
+    return B, Hq, d, Hkv
+
+
+def decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits=0) -> int:
+    return int(load_library().yr_decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits))
+
+
+def attn_fwd_decode_sinkwindow(cfg: RopeConfig, q, k_cache, v_cache, n_valid, ring_start,
+                               sink: int, window: int, num_splits: int = 0, out=None, lse=None,
+                               return_lse: bool = False, workspace=None, stream=None):
+    """q [B, Hq, d] bf16; caches [B, Hkv, sink + window, d] bf16 (contiguous);
+    n_valid / ring_start int32 [B].  Returns o [B, Hq, d] (and lse [B, Hq])."""
+    lib = load_library()
+    B, Hq, d, Hkv = _check_decode_args(q, k_cache, v_cache, n_valid, ring_start, sink, window, out, lse)
     o = torch.empty_like(q) if out is None else out
     if return_lse and lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
@@ -388,14 +406,18 @@ def attn_fwd_decode_sinkwindow_noalloc(cfg: RopeConfig, q, k_cache, v_cache, n_v
     call).  ``out`` and ``lse`` are the caller's; nothing is allocated when
     both are given."""
     lib = load_library()
-    B, Hq, d = q.shape
-    Hkv = k_cache.shape[1]
+    B, Hq, d, Hkv = _check_decode_args(q, k_cache, v_cache, n_valid, ring_start, sink, window, out, lse)
     o = torch.empty_like(q) if out is None else out
     c = cfg.c()
     _check(lib.attn_fwd_decode_sinkwindow_noalloc(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(n_valid), _ptr(ring_start),
         B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits), _stream(stream)))
     return o
+
+
+def kernel_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().yr_kernel_launch_count())
 
 
 def sync_status(stream=None):

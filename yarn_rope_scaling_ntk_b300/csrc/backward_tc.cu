@@ -777,7 +777,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   bwd_kv_kernel<D><<<(unsigned)(p.n_tiles * a.B * a.Hkv), kThreads, smem, st>>>(mq, mk, mv, mdo, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launched(1)) != cudaSuccess) return e;
   // dQ
   p.hgroup = heads_per_group(a.B * a.Hq);
   p.out_a = a.dq; p.out_b = nullptr;
@@ -786,7 +786,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& a, cudaStream_t st) {
   e = cudaFuncSetAttribute(bwd_q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   bwd_q_kernel<D><<<(unsigned)(p.n_tiles * a.B * a.Hq), kThreads, smem, st>>>(mq, mk, mv, mdo, p);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace
@@ -805,7 +805,7 @@ cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, 
     dsum_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float*>(dout), static_cast<const float*>(o),
                                                          dsum, lse, lse2, B, H, S, d, ds[0], ds[1], ds[2], os[0], os[1],
                                                          os[2]);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {

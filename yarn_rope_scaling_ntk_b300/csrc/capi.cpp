@@ -121,6 +121,23 @@ yr_status build_rope_freqs(const yr_rope_cfg* cfg, int d, RopeFreqs* out) {
   return YR_OK;
 }
 
+// The shape and configuration checks of the decode entry points, in the
+// order they report errors (no pointer is dereferenced).
+yr_status decode_check_shape(const char* who, const yr_rope_cfg* cfg, int32_t B, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t sink, int32_t window, int32_t num_splits, RopeFreqs* f) {
+  if (!cfg) return fail(YR_ERR_INVALID_ARG, "%s: cfg is NULL", who);
+  if (B < 0 || Hq < 0 || Hkv < 0) return fail(YR_ERR_INVALID_ARG, "negative shape");
+  if (d != 64 && d != 128) return fail(YR_ERR_UNSUPPORTED, "decode head dimension %d (64 or 128)", d);
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return fail(YR_ERR_INVALID_ARG, "Hq %% Hkv != 0");
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(YR_ERR_UNSUPPORTED, "decode supports Hq/Hkv in {1, 2, 4, 8}, got %d", G);
+  if (sink < 0 || window < 1) return fail(YR_ERR_INVALID_ARG, "sink must be >= 0 and window >= 1");
+  if ((int64_t)sink + window > (1 << 24)) return fail(YR_ERR_INVALID_ARG, "cache above 2^24 entries");
+  if (num_splits > 4096) return fail(YR_ERR_INVALID_ARG, "num_splits above 4096");
+  return build_rope_freqs(cfg, d, f);
+}
+
 }  // namespace yr
 
 using namespace yr;
@@ -483,23 +500,14 @@ size_t yr_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, 
   return (size_t)splits * B * Hq * (d + 2) * sizeof(float);
 }
 
+
 static yr_status decode_impl(const char* who, const yr_rope_cfg* cfg, const void* q, const void* k_cache,
                              const void* v_cache, int fp8, const float* k_scale, const float* v_scale,
                              const int32_t* n_valid, const int32_t* ring_start, int32_t B, int32_t Hq,
                              int32_t Hkv, int32_t d, int32_t sink, int32_t window, void* o, float* lse,
                              int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!cfg) return fail(YR_ERR_INVALID_ARG, "%s: cfg is NULL", who);
-  if (B < 0 || Hq < 0 || Hkv < 0) return fail(YR_ERR_INVALID_ARG, "negative shape");
-  if (d != 64 && d != 128) return fail(YR_ERR_UNSUPPORTED, "decode head dimension %d (64 or 128)", d);
-  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return fail(YR_ERR_INVALID_ARG, "Hq %% Hkv != 0");
-  const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8)
-    return fail(YR_ERR_UNSUPPORTED, "decode supports Hq/Hkv in {1, 2, 4, 8}, got %d", G);
-  if (sink < 0 || window < 1) return fail(YR_ERR_INVALID_ARG, "sink must be >= 0 and window >= 1");
-  if ((int64_t)sink + window > (1 << 24)) return fail(YR_ERR_INVALID_ARG, "cache above 2^24 entries");
-  if (num_splits > 4096) return fail(YR_ERR_INVALID_ARG, "num_splits above 4096");
   RopeFreqs f;
-  yr_status st = build_rope_freqs(cfg, d, &f);
+  yr_status st = decode_check_shape(who, cfg, B, Hq, Hkv, d, sink, window, num_splits, &f);
   if (st != YR_OK) return st;
   if (B == 0) return YR_OK;
   if (!q || !k_cache || !v_cache || !n_valid || !ring_start || !o)

@@ -509,10 +509,10 @@ cudaError_t launch_dg(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st
   cudaError_t e0 = cudaFuncSetAttribute(decode_kernel<D, G, EB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e0 != cudaSuccess) return e0;
   decode_kernel<D, G, EB><<<grid, kThreads, smem, st>>>(a, f);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launched(1);
   if (e != cudaSuccess || a.splits == 1) return e;
   decode_merge_kernel<<<(unsigned)(a.B * a.Hq), 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace
@@ -590,9 +590,14 @@ extern "C" yr_status attn_fwd_decode_sinkwindow_noalloc(
     const yr_rope_cfg* cfg, const void* q, const void* k_cache, const void* v_cache, const int32_t* n_valid,
     const int32_t* ring_start, int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t sink, int32_t window,
     void* o, float* lse, int32_t num_splits, void* stream) {
+  yr::clear_error();
+  // the same argument errors as the workspace entry point, before the size test
+  yr::RopeFreqs f;
+  const yr_status st = yr::decode_check_shape("attn_fwd_decode_sinkwindow_noalloc", cfg, B, Hq, Hkv, d, sink,
+                                              window, num_splits, &f);
+  if (st != YR_OK) return st;
   const size_t need = yr_decode_workspace_bytes(B, Hq, Hkv, d, sink, window, num_splits);
   if (need > yr::kNoAllocScratchBytes) {
-    yr::clear_error();
     return yr::fail(YR_ERR_INVALID_ARG,
                     "attn_fwd_decode_sinkwindow_noalloc: %zu bytes of split scratch needed, above its fixed "
                     "%zu-byte array; use fewer splits or attn_fwd_decode_sinkwindow with a workspace",
@@ -602,7 +607,6 @@ extern "C" yr_status attn_fwd_decode_sinkwindow_noalloc(
   if (need > 0) {
     scratch = yr::decode_scratch_address();
     if (!scratch) {
-      yr::clear_error();
       return yr::fail(YR_ERR_CUDA, "attn_fwd_decode_sinkwindow_noalloc: device scratch address unavailable");
     }
   }

@@ -28,6 +28,11 @@ yr_status compute_inv_freq(const yr_rope_cfg* cfg, int d, double* theta, int8_t*
 // Host: the device table built from compute_inv_freq.
 yr_status build_rope_freqs(const yr_rope_cfg* cfg, int d, RopeFreqs* out);
 
+// Host: the shape and configuration checks shared by the decode entry points;
+// fills the frequency table on success.
+yr_status decode_check_shape(const char* who, const yr_rope_cfg* cfg, int32_t B, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t sink, int32_t window, int32_t num_splits, RopeFreqs* f);
+
 // Error text helpers (thread-local message).
 yr_status fail(yr_status st, const char* fmt, ...);
 void clear_error();
@@ -35,6 +40,10 @@ yr_status cuda_fail(cudaError_t e, const char* what);
 
 // Address of the device status word (per device), set by bounded waits.
 int* device_status_word();
+
+// After a kernel launch: the launch status (cudaGetLastError), and on
+// success `n` more launches on the library's launch counter.
+cudaError_t launched(int n);
 
 // Number of SMs of the current device.
 int sm_count();

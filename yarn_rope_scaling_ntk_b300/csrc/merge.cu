@@ -100,7 +100,7 @@ cudaError_t launch_fill_empty(void* o, int out_bf16, float* lse, int B, int H, i
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   fill_empty_kernel<<<(unsigned)blocks, 256, 0, st>>>(o, out_bf16, lse, B, H, S, d, os[0], os[1], os[2]);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st) {
@@ -114,7 +114,7 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st) {
   else if (ch <= 4) merge_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(a);
   else if (ch <= 8) merge_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(a);
   else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace yr

@@ -575,7 +575,7 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   const int64_t blocks = (int64_t)p.n_pairs * a.B * a.Hq;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   prefill_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace

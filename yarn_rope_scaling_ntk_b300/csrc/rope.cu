@@ -124,7 +124,7 @@ cudaError_t launch_rope(const RopeLaunch& a, const RopeFreqs& f, cudaStream_t st
     rope_kernel<float, float, true><<<blocks, 256, 0, st>>>(a, f);
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace yr

@@ -1,5 +1,10 @@
 // Device error word set by kernels whose bounded waits give up; read and
-// cleared by yr_sync_status().
+// cleared by yr_sync_status().  The device addresses are looked up once per
+// device and cached; the cache assumes the CUDA context of a device lives as
+// long as the process (the library is not to be used across a device reset).
+#include <atomic>
+#include <mutex>
+
 #include "internal.h"
 
 namespace yr {
@@ -7,9 +12,11 @@ namespace yr {
 __device__ int g_status_word = 0;
 
 int* device_status_word() {
+  static std::mutex mu;
   static int* cached[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
@@ -18,4 +25,14 @@ int* device_status_word() {
   return cached[dev];
 }
 
+static std::atomic<unsigned long long> g_launches{0};
+
+cudaError_t launched(int n) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed);
+  return e;
+}
+
 }  // namespace yr
+
+extern "C" uint64_t yr_kernel_launch_count(void) { return yr::g_launches.load(std::memory_order_relaxed); }
