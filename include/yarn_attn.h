@@ -335,6 +335,21 @@ yr_status attn_fwd_decode_sinkwindow_noalloc(const yr_rope_cfg* cfg, const void*
  * CUDA error, YR_OK otherwise. */
 yr_status yr_sync_status(void* stream);
 
+/* Test hook for the failure path: host-controlled fault injection (the pages
+ * have no counterpart; not for production use).  While set, the decode and
+ * prefill kernels bound their first-level waits by wait_limit_cycles SM
+ * cycles (0: the default, 4e9, about 2 s at the maximum clock) and, when
+ * skip_unit >= 0, their load producers never issue the copies of that load
+ * unit (decode: cache chunk skip_unit of each slice; prefill: K/V load unit
+ * skip_unit of each CTA, unit 0 being the first K tile), so the wait on it
+ * runs out.  A kernel whose wait runs out records the code that
+ * yr_sync_status() reports as YR_ERR_TIMEOUT, lets the copies and products
+ * it issued finish, frees its tensor memory and returns; the outputs of that
+ * call are undefined and the device stays usable.  The setting is process-wide and stays
+ * until changed: yr_debug_inject_wait_fault(0, -1) turns it off.
+ * wait_limit_cycles < 0 or skip_unit < -1 returns YR_ERR_INVALID_ARG. */
+yr_status yr_debug_inject_wait_fault(int64_t wait_limit_cycles, int32_t skip_unit);
+
 /* Number of kernels the library has launched in this process so far, over
  * every entry point and device (each successful launch counts once).  Host
  * only; for counting the launches inside a timed region.  Not part of the

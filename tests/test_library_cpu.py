@@ -209,3 +209,19 @@ def test_noalloc_python_wrapper_validates_like_its_sibling(lib):
         with pytest.raises(ValueError):
             api.attn_fwd_decode_sinkwindow_noalloc(cfg, a["q"], a["k_cache"], a["v_cache"], a["n_valid"],
                                                    a["ring_start"], sink, win, out=a["out"], lse=a["lse"])
+
+
+def test_fault_injection_hook_checks_its_arguments(lib):
+    assert lib.yr_debug_inject_wait_fault(-1, -1) == 1
+    assert lib.yr_debug_inject_wait_fault(0, -2) == 1
+    assert lib.yr_debug_inject_wait_fault(1000, 3) == 0
+    assert lib.yr_debug_inject_wait_fault(0, -1) == 0  # off again
+
+
+def test_launch_counter_does_not_count_refused_calls(lib):
+    n = lib.yr_kernel_launch_count()
+    cfg = api.RopeConfig(kind="yarn", head_dim=96, L_train=4096, s=4.0).c()
+    assert lib.attn_fwd_prefill(ctypes.byref(cfg), None, None, None, None, None, 1, 1, 4, 4, 128, 96,
+                                _i64(0, 0, 0), _i64(0, 0, 0), _i64(0, 0, 0), _i64(0, 0, 0), 0, 0, 0,
+                                1, 0.0, None, 0, None) == 2
+    assert lib.yr_kernel_launch_count() == n

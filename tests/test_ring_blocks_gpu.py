@@ -192,3 +192,31 @@ def test_ring_blocks_full_size_sampled_rows():
         got.append(f64(final[0, h, rws]))
         want.append(o)
     assert_attn_close(np.concatenate(got), np.concatenate(want), "ring blocks 128K")
+
+
+@pytest.mark.parametrize("world,mask,sink,window,Hq,Hkv", [(4, "causal", 0, 0, 4, 2), (3, "none", 0, 0, 2, 2),
+                                                           (4, "sink_window", 4, 300, 4, 1)])
+def test_ring_driver_all_ranks_in_one_process(world, mask, sink, window, Hq, Hkv):
+    """The ring driver's per-rank computation with the library's kernels, all
+    ranks of a ring run in lock step on one GPU (the exchange is a hand-over
+    of the rotated blocks): every row of every rank against the oracle, and
+    against the fused call in ring order."""
+    need_cuda()
+    from yarn_rope_scaling_ntk_b300 import ring
+    B, bs, d = 1, 256, 128
+    S = bs * world
+    g = torch.Generator(device="cuda").manual_seed(4100 + world)
+    q = torch.randn(B, Hq, S, d, generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn(B, Hkv, S, d, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(B, Hkv, S, d, generator=g, device="cuda").to(torch.bfloat16)
+    blocks = lambda t: [t[:, :, i * bs:(i + 1) * bs].contiguous() for i in range(world)]
+    res = ring.ring_attention_one_process(_cfg(d), blocks(q), blocks(k), blocks(v), mask=mask, sink=sink,
+                                          window=window)
+    api.sync_status()
+    o = torch.cat([r[0] for r in res], dim=2)
+    lse = torch.cat([r[1] for r in res], dim=2)
+    want_o, want_l = _oracle_block(q, k, v, 0, 0, mask, sink, window, d, Hq // Hkv)
+    assert_attn_close(f64(o), want_o, f"ring driver, {world} ranks")
+    assert_lse_close(f64(lse), want_l, f"ring driver, {world} ranks")
+    fused = api.attn_fwd_prefill(_cfg(d), q, k, v, mask=mask, sink=sink, window=window, ring_blocks=world)
+    assert (fused.float() - o.float()).abs().max().item() < 2e-2

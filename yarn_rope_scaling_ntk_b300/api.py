@@ -116,6 +116,7 @@ def load_library():
                                                      I32, I32, _P, _P, I32, _P]),
         "yr_sync_status": (I32, [_P]),
         "yr_kernel_launch_count": (ctypes.c_uint64, []),
+        "yr_debug_inject_wait_fault": (I32, [ctypes.c_int64, I32]),
         "yr_last_error_message": (ctypes.c_char_p, []),
         "yr_version": (ctypes.c_char_p, []),
     }
@@ -413,6 +414,13 @@ def attn_fwd_decode_sinkwindow_noalloc(cfg: RopeConfig, q, k_cache, v_cache, n_v
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(n_valid), _ptr(ring_start),
         B, Hq, Hkv, d, int(sink), int(window), _ptr(o), _ptr(lse), int(num_splits), _stream(stream)))
     return o
+
+
+def debug_inject_wait_fault(wait_limit_cycles: int = 0, skip_unit: int = -1):
+    """Test hook for the failure path: bound the decode and prefill kernels'
+    waits by ``wait_limit_cycles`` and make their producers skip load unit
+    ``skip_unit``; ``(0, -1)`` turns it off.  Process-wide."""
+    _check(load_library().yr_debug_inject_wait_fault(int(wait_limit_cycles), int(skip_unit)))
 
 
 def kernel_launch_count() -> int:

@@ -194,11 +194,14 @@ yr_status rope_apply(const yr_rope_cfg* cfg, const void* x, void* y, int32_t dty
   if (x == y && memcmp(x_strides, y_strides, 3 * sizeof(int64_t)) != 0)
     return fail(YR_ERR_INVALID_ARG, "in-place rope_apply needs identical strides");
   RopeLaunch a;
-  a.x = x; a.y = y; a.in_bf16 = a.out_bf16 = dtype == YR_BF16;
-  a.B = B; a.H = H; a.S = S; a.d = d;
-  for (int i = 0; i < 3; ++i) { a.xs[i] = x_strides[i]; a.ys[i] = y_strides[i]; }
-  a.pos0 = pos0; a.positions = positions; a.apply_mscale = apply_mscale != 0;
-  a.precise = dtype == YR_F32;
+  memset(&a, 0, sizeof(a));
+  a.n_seg = 1;
+  RopeSegment& sg = a.seg[0];
+  sg.x = x; sg.y = y; sg.H = H; sg.S = S; sg.pos0 = pos0;
+  for (int i = 0; i < 3; ++i) { sg.xs[i] = x_strides[i]; sg.ys[i] = y_strides[i]; }
+  a.in_bf16 = a.out_bf16 = dtype == YR_BF16;
+  a.B = B; a.d = d;
+  a.positions = positions; a.apply_mscale = apply_mscale != 0;
   cudaError_t e = launch_rope(a, f, as_stream(stream));
   return e == cudaSuccess ? YR_OK : cuda_fail(e, "rope_apply launch");
 }
@@ -293,29 +296,29 @@ static yr_status prefill_impl(const char* who, const yr_rope_cfg* cfg, const voi
 
   // Rotated bfloat16 copies in the workspace, each [B, H, rows, d]
   // contiguous: Q (rotated at q_pos0 + row), K (rotated at k_pos0 + key),
-  // and V (converted) for float32 inputs.
+  // and V (converted) for float32 inputs -- one launch for all of them.
   char* ws = static_cast<char*>(workspace);
   size_t off = 0;
+  RopeLaunch ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.in_bf16 = in_dtype == YR_BF16; ra.out_bf16 = 1;
+  ra.B = B; ra.d = d;
   auto prep = [&](const void* src, const int64_t* src_s, int H, int rows, int pos0, bool rotate,
-                  const void** dst, int64_t* dst_s) -> cudaError_t {
+                  const void** dst, int64_t* dst_s) {
     void* out = ws + off;
     const int64_t hs = (int64_t)rows * d;
     off += (size_t)B * H * hs * 2;
-    RopeLaunch a;
-    memset(&a, 0, sizeof(a));
-    a.x = src; a.y = out; a.in_bf16 = in_dtype == YR_BF16; a.out_bf16 = 1;
-    a.B = B; a.H = H; a.S = rows; a.d = d; a.pos0 = pos0;
+    RopeSegment& sg = ra.seg[ra.n_seg++];
+    sg.x = src; sg.y = out; sg.H = H; sg.S = rows; sg.pos0 = pos0; sg.identity = rotate ? 0 : 1;
     dst_s[0] = (int64_t)H * hs; dst_s[1] = hs; dst_s[2] = d;
-    for (int i = 0; i < 3; ++i) { a.xs[i] = src_s[i]; a.ys[i] = dst_s[i]; }
-    RopeFreqs ff = f;
-    if (!rotate) ff.identity = 1;
+    for (int i = 0; i < 3; ++i) { sg.xs[i] = src_s[i]; sg.ys[i] = dst_s[i]; }
     *dst = out;
-    return launch_rope(a, ff, cs);
   };
   if (prefill_needs_q_copy(in_dtype, cfg)) {
-    cudaError_t e = prep(q, q_strides, Hq, Sq, q_pos0, true, &p.q, p.qs);
-    if (e == cudaSuccess) e = prep(k, k_strides, Hkv, Skv, k_pos0, true, &p.k, p.ks);
-    if (e == cudaSuccess && in_dtype == YR_F32) e = prep(v, v_strides, Hkv, Skv, 0, false, &p.v, p.vs);
+    prep(q, q_strides, Hq, Sq, q_pos0, true, &p.q, p.qs);
+    prep(k, k_strides, Hkv, Skv, k_pos0, true, &p.k, p.ks);
+    if (in_dtype == YR_F32) prep(v, v_strides, Hkv, Skv, 0, false, &p.v, p.vs);
+    cudaError_t e = launch_rope(ra, f, cs);
     if (e != cudaSuccess) return cuda_fail(e, "attention rotation pass");
   }
   cudaError_t e = launch_prefill(p, cs);
@@ -437,33 +440,31 @@ yr_status attn_bwd(const yr_rope_cfg* cfg, const void* q, const void* k, const v
   size_t off = 0;
   BwdLaunch a;
   memset(&a, 0, sizeof(a));
-  auto prep = [&](const void* src, const int64_t* src_s, int H, bool rotate, const void** dst,
-                  int64_t* dst_s) -> cudaError_t {
+  // rotated Q and K (and converted V, dO for float32 inputs): one launch
+  RopeLaunch ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.in_bf16 = in_dtype == YR_BF16; ra.out_bf16 = 1;
+  ra.B = B; ra.d = d;
+  auto prep = [&](const void* src, const int64_t* src_s, int H, bool rotate, const void** dst, int64_t* dst_s) {
     void* out = ws + off;
     const int64_t hs = (int64_t)S * d;
     off += align16((size_t)B * H * hs * 2);
-    RopeLaunch r;
-    memset(&r, 0, sizeof(r));
-    r.x = src; r.y = out; r.in_bf16 = in_dtype == YR_BF16; r.out_bf16 = 1;
-    r.B = B; r.H = H; r.S = S; r.d = d;
+    RopeSegment& sg = ra.seg[ra.n_seg++];
+    sg.x = src; sg.y = out; sg.H = H; sg.S = S; sg.identity = rotate ? 0 : 1;
     dst_s[0] = (int64_t)H * hs; dst_s[1] = hs; dst_s[2] = d;
-    for (int i = 0; i < 3; ++i) { r.xs[i] = src_s[i]; r.ys[i] = dst_s[i]; }
-    RopeFreqs ff = f;
-    if (!rotate) ff.identity = 1;
+    for (int i = 0; i < 3; ++i) { sg.xs[i] = src_s[i]; sg.ys[i] = dst_s[i]; }
     *dst = out;
-    return launch_rope(r, ff, cs);
   };
-  cudaError_t e = prep(q, q_strides, Hq, true, &a.q, a.qs);
-  if (e == cudaSuccess) e = prep(k, k_strides, Hkv, true, &a.k, a.ks);
-  if (e == cudaSuccess) {
-    if (in_dtype == YR_F32) {
-      e = prep(v, v_strides, Hkv, false, &a.v, a.vs);
-      if (e == cudaSuccess) e = prep(dout, do_strides, Hq, false, &a.dout, a.dos);
-    } else {
-      a.v = v; a.dout = dout;
-      for (int i = 0; i < 3; ++i) { a.vs[i] = v_strides[i]; a.dos[i] = do_strides[i]; }
-    }
+  prep(q, q_strides, Hq, true, &a.q, a.qs);
+  prep(k, k_strides, Hkv, true, &a.k, a.ks);
+  if (in_dtype == YR_F32) {
+    prep(v, v_strides, Hkv, false, &a.v, a.vs);
+    prep(dout, do_strides, Hq, false, &a.dout, a.dos);
+  } else {
+    a.v = v; a.dout = dout;
+    for (int i = 0; i < 3; ++i) { a.vs[i] = v_strides[i]; a.dos[i] = do_strides[i]; }
   }
+  cudaError_t e = launch_rope(ra, f, cs);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd rotation pass");
   float* dsum = reinterpret_cast<float*>(ws + off);
   off += align16((size_t)B * Hq * S * 4);

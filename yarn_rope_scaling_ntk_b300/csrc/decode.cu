@@ -33,6 +33,7 @@ using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
 using tc::mbar_wait_drain;
+using tc::bulk_g2s;
 using tc::smem_u32;
 
 constexpr int kWarps = 8;                    // compute warps
@@ -101,30 +102,6 @@ __device__ __forceinline__ void load_cache(const uint8_t* p, float (&x)[N]) {
   else load_e4m3<N>(p, x);
 }
 
-// Two float32 lanes at once (sm_100 family packed arithmetic); each lane is
-// an ordinary round-to-nearest float32 fma / multiply.
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
-                                     float c1) {
-  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
-      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
-      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}\n"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 template <int D, int G, int EB>
 __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(DecodeLaunch a, RopeFreqs f) {
   constexpr int PPT = G >= 2 ? 4 : 8;
@@ -174,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
       int c = 0;
       for (int jc = j0; jc < j1; jc += CK, ++c) {
         const int s = c % NSTG;
-        if (!mbar_wait(&empty[s], ((c / NSTG) & 1) ^ 1, &abort_flag, status, 41)) break;
+        if (!mbar_wait(&empty[s], ((c / NSTG) & 1) ^ 1, &abort_flag, status, 41, a.wait_limit)) break;
+        if (c == a.skip_unit) continue;  // fault injection: this chunk is never loaded
         const int nk = min(CK, j1 - jc);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nk * ROW));
         for (int j = jc; j < jc + nk;) {
@@ -195,9 +173,12 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
         }
         ++issued[s];
       }
-      if (abort_flag)
-        for (int s = 0; s < NSTG; ++s)
-          if (issued[s]) mbar_wait_drain(&full[s], (issued[s] - 1) & 1, 200000000ll);
+      // Every copy issued lands before the stage buffers are reused for the
+      // merge below, also when the compute warps gave up on a chunk after
+      // the last one was issued (the last phase of each stage is waited for;
+      // the stage's barrier cannot move past it).
+      for (int s = 0; s < NSTG; ++s)
+        if (issued[s]) mbar_wait_drain(&full[s], (issued[s] - 1) & 1, 200000000ll);
     }
     __syncwarp();
     __syncthreads();
@@ -278,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
   int c = 0;
   for (int jc = j0; jc < j1; jc += CK, ++c) {
     const int s = c % NSTG;
-    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (c / NSTG) & 1, &abort_flag, status, 42));
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (c / NSTG) & 1, &abort_flag, status, 42, a.wait_limit));
     if (!ok) break;
     const uint8_t* stK = sK + s * Sh::STAGE;
     const uint8_t* stV = sV + s * Sh::STAGE;
@@ -521,6 +502,9 @@ cudaError_t launch_decode(const DecodeLaunch& a_in, const RopeFreqs& f, cudaStre
   DecodeLaunch a = a_in;
   a.status = device_status_word();
   if (!a.status) return cudaErrorInvalidValue;
+  const FaultInjection fi = fault_injection();
+  a.wait_limit = fi.wait_limit;
+  a.skip_unit = fi.skip_unit;
   const int G = a.Hq / a.Hkv;
   if (a.fp8) {
     if (a.d == 128) {

@@ -45,6 +45,17 @@ int* device_status_word();
 // success `n` more launches on the library's launch counter.
 cudaError_t launched(int n);
 
+// Host-controlled fault injection for the failure-path tests, off unless
+// yr_debug_inject_wait_fault() set it: the bound of the decode and prefill
+// kernels' first-level waits, and the load unit (a chunk of the decode cache,
+// a K/V unit of the attention) whose copies their producer never issues, so
+// that the wait on it runs out.  Off: 4e9 cycles and -1.
+struct FaultInjection {
+  long long wait_limit;
+  int skip_unit;
+};
+FaultInjection fault_injection();
+
 // Number of SMs of the current device.
 int sm_count();
 // TMA map of a [B, H, S, D] bfloat16 tensor (element strides b, h, s): 4-D,
@@ -52,16 +63,29 @@ int sm_count();
 bool make_map(CUtensorMap* map, const void* base, int B, int H, int S, int D, const int64_t st[3]);
 
 // ---- launches (kernel files) ----------------------------------------------
-struct RopeLaunch {
+// One tensor of a rotation pass: [B, H, S, d] rows at positions pos0 + s
+// (or the launch's explicit positions), written to y.
+struct RopeSegment {
   const void* x;
   void* y;
-  int in_bf16, out_bf16;
-  int B, H, S, d;
-  int64_t xs[3], ys[3];
+  int H, S;
+  int64_t xs[3], ys[3];  // element strides (batch, head, position)
   int pos0;
-  const int32_t* positions;
+  int identity;  // 1: no rotation (a conversion, and mscale when asked)
+  int64_t tile0;  // set by the launcher: first tile of this segment
+};
+constexpr int kMaxRopeSegments = 4;
+struct RopeLaunch {
+  RopeSegment seg[kMaxRopeSegments];
+  int n_seg;
+  int in_bf16, out_bf16;  // float32 -> float32 uses the precise angle path
+  int B, d;
+  const int32_t* positions;  // explicit positions of row s (one segment), or NULL
   int apply_mscale;
-  int precise;  // 1: sincospif-based angles (float32 outputs)
+  // set by the launcher
+  int rows_per_tile;
+  int64_t n_tiles;
+  int* status;
 };
 cudaError_t launch_rope(const RopeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
@@ -80,6 +104,8 @@ struct DecodeLaunch {
   int B, Hq, Hkv, d, sink, window, splits;
   float scale_log2;
   int* status;  // device status word (set by the launcher)
+  long long wait_limit;  // first-level wait bound in cycles (set by the launcher)
+  int skip_unit;         // fault injection: cache chunk never loaded (-1: none)
 };
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 

@@ -55,6 +55,12 @@ constexpr uint32_t kRegsControl = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Waves of CTAs per scheduling group of KV heads (see the CTA order below):
+// the K/V of a group's heads stays in L2 while its CTAs stream it.
+#ifndef YR_PREFILL_SCHED_WAVES
+#define YR_PREFILL_SCHED_WAVES 3
+#endif
+constexpr int kSchedWaves = YR_PREFILL_SCHED_WAVES;
 
 struct TcParams {
   int B, Hq, Hkv, group, n_pairs;
@@ -67,6 +73,8 @@ struct TcParams {
   float* lse;
   int out_bf16;
   int* status;
+  long long wait_limit;  // first-level wait bound in cycles
+  int skip_unit;         // fault injection: load unit never issued (-1: none)
 };
 
 // Key chunks in ring order for one CTA (two query tiles a and b): ring
@@ -244,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Walk walk;
   walk.init(p, pair);
+  int uses[NS] = {0};  // producer: load units issued per stage
 
   if (warp >= 8) {
     reg_dealloc<kRegsControl>();
@@ -262,29 +271,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // otherwise, on barrier u % NS.  K(c) lives in K buffer c % NS and
         // V(c) in V buffer c % NS, so unit u reuses exactly the buffers of
         // unit u - NS and waits for that unit's release.
-        int uses[NS] = {0};
         bool v0, v1;
         int prev = -1;
         int cur = walk.next(v0, v1);
         for (int u = 0; cur >= 0 || prev >= 0; ++u) {
           const int s = u % NS;
-          if (!mbar_wait(&kv_empty[s], ((u / NS) & 1) ^ 1, &abort_flag, p.status, 11)) break;
-          mbar_arrive_expect_tx(&kv_full[s], (prev >= 0 ? C::kTile : 0) + (cur >= 0 ? C::kTile : 0));
-          if (prev >= 0)
-            for (int a = 0; a < ATOMS; ++a)
-              tma_load_4d(sV + ((u - 1) % NS) * C::kTile + a * ATOM_BYTES, &tv, &kv_full[s], a * 64, prev, hkv, b);
-          if (cur >= 0)
-            for (int a = 0; a < ATOMS; ++a)
-              tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &kv_full[s], a * 64, cur, hkv, b);
-          ++uses[s];
+          if (!mbar_wait(&kv_empty[s], ((u / NS) & 1) ^ 1, &abort_flag, p.status, 11, p.wait_limit)) break;
+          if (u != p.skip_unit) {  // (fault injection: a skipped unit is never loaded)
+            mbar_arrive_expect_tx(&kv_full[s], (prev >= 0 ? C::kTile : 0) + (cur >= 0 ? C::kTile : 0));
+            if (prev >= 0)
+              for (int a = 0; a < ATOMS; ++a)
+                tma_load_4d(sV + ((u - 1) % NS) * C::kTile + a * ATOM_BYTES, &tv, &kv_full[s], a * 64, prev, hkv, b);
+            if (cur >= 0)
+              for (int a = 0; a < ATOMS; ++a)
+                tma_load_4d(sK + s * C::kTile + a * ATOM_BYTES, &tk, &kv_full[s], a * 64, cur, hkv, b);
+            ++uses[s];
+          }
           prev = cur;
           cur = cur >= 0 ? walk.next(v0, v1) : -1;
-        }
-        if (abort_flag) {
-          // let the copies already issued land before the CTA exits
-          mbar_wait_drain(&q_full, 0, 200000000ll);
-          for (int s = 0; s < NS; ++s)
-            if (uses[s]) mbar_wait_drain(&kv_full[s], (uses[s] - 1) & 1, 200000000ll);
         }
       }
       __syncwarp();
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         };
         auto wait = [&](uint64_t* bar, uint32_t par, int code) -> bool {
-          return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code));
+          return __all_sync(0xffffffffu, mbar_wait(bar, par, &abort_flag, p.status, code, p.wait_limit));
         };
         bool ok = wait(&q_full, 0, 21);
         int pv_count[2] = {0, 0};
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n0 = walk.next(v0, v1); n0 >= 0; n0 = walk.next(v0, v1)) {
       if (!(wg ? v1 : v0)) continue;
       // warp-uniform decisions: tcgen05.ld / st are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], i & 1, &abort_flag, p.status, 31));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], i & 1, &abort_flag, p.status, 31, p.wait_limit));
       if (!ok) break;
       tc_fence_after();
       uint32_t raw[4][32];
@@ -492,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O / l -> global, lse
     if (__all_sync(0xffffffffu, ok && !abort_flag)) {
       bool have = true;
-      if (i > 0) have = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], 0, &abort_flag, p.status, 33));
+      if (i > 0)
+        have = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], 0, &abort_flag, p.status, 33, p.wait_limit));
       tc_fence_after();
       if (have) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -539,6 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // After an abort the copies the producer issued land before the CTA exits;
+  // the flag is final here, since every role has left its loop.  (Without
+  // an abort the MMA warp has waited for every unit issued.)
+  if (warp == kLoadWarp && lane == 0 && abort_flag) {
+    mbar_wait_drain(&q_full, 0, 200000000ll);
+    for (int s = 0; s < NS; ++s)
+      if (uses[s]) mbar_wait_drain(&kv_full[s], (uses[s] - 1) & 1, 200000000ll);
+  }
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -554,10 +567,10 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   p.Sq = a.Sq; p.Skv = a.Skv; p.qp0 = a.q_pos0; p.kp0 = a.k_pos0;
   p.n_pairs = (a.Sq + 2 * BM - 1) / (2 * BM);
   {
-    // enough KV heads per scheduling group for about three waves of CTAs
+    // enough KV heads per scheduling group for about kSchedWaves waves of CTAs
     const int per_kv = p.n_pairs * p.group;
     const int n_kv = a.B * a.Hkv;
-    int k = (3 * sm_count() + per_kv - 1) / per_kv;
+    int k = (kSchedWaves * sm_count() + per_kv - 1) / per_kv;
     p.kv_per_sched = k < 1 ? 1 : (k > n_kv ? n_kv : k);
   }
   p.mask = a.mask; p.sink = a.sink; p.window = a.window; p.ring_blocks = a.ring_blocks;
@@ -569,6 +582,9 @@ cudaError_t launch_d(const PrefillLaunch& a, cudaStream_t st) {
   p.out_bf16 = a.out_bf16;
   p.status = device_status_word();
   if (!p.status) return cudaErrorInvalidValue;
+  const FaultInjection fi = fault_injection();
+  p.wait_limit = fi.wait_limit;
+  p.skip_unit = fi.skip_unit;
   const int smem = Cfg<D>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

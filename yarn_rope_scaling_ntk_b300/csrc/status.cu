@@ -26,6 +26,13 @@ int* device_status_word() {
 }
 
 static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<long long> g_wait_limit{0};
+static std::atomic<int> g_skip_unit{-1};
+
+FaultInjection fault_injection() {
+  const long long w = g_wait_limit.load(std::memory_order_relaxed);
+  return {w > 0 ? w : 4000000000ll, g_skip_unit.load(std::memory_order_relaxed)};
+}
 
 cudaError_t launched(int n) {
   const cudaError_t e = cudaGetLastError();
@@ -34,5 +41,14 @@ cudaError_t launched(int n) {
 }
 
 }  // namespace yr
+
+extern "C" yr_status yr_debug_inject_wait_fault(int64_t wait_limit_cycles, int32_t skip_unit) {
+  yr::clear_error();
+  if (wait_limit_cycles < 0 || skip_unit < -1)
+    return yr::fail(YR_ERR_INVALID_ARG, "yr_debug_inject_wait_fault: wait_limit_cycles >= 0, skip_unit >= -1");
+  yr::g_wait_limit.store(wait_limit_cycles, std::memory_order_relaxed);
+  yr::g_skip_unit.store(skip_unit, std::memory_order_relaxed);
+  return YR_OK;
+}
 
 extern "C" uint64_t yr_kernel_launch_count(void) { return yr::g_launches.load(std::memory_order_relaxed); }
