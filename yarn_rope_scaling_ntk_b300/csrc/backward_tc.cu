@@ -112,14 +112,6 @@ __device__ __forceinline__ bool tile_needs_mask(const BwdParams& p, int m0, int 
   return p.mask == YR_MASK_SINK_WINDOW && n1 >= p.sink && m1 - max(n0, p.sink) >= p.window;
 }
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Query tiles that see key tile kt: [lo, hi] (hi < lo when none).
 __device__ __forceinline__ void query_tiles(const BwdParams& p, int kt, int& lo, int& hi) {
   lo = p.mask == YR_MASK_NONE ? 0 : kt;
