@@ -46,26 +46,29 @@ CSRC = os.path.join(ROOT, "yarn_rope_scaling_ntk_b300", "csrc")
 # the kernel's source files at capture time.  A kernel whose sources changed
 # since reports null.  The commands are in profiles/.
 KERNEL_SOURCES = {
-    "prefill_tc": ("prefill_tc.cu", "tc_ptx.cuh"),
+    "prefill_tc": ("prefill_tc.cu", "tc_ptx.cuh", "common.cuh"),
     "decode": ("decode.cu", "tc_ptx.cuh", "common.cuh"),
-    "rope": ("rope.cu", "common.cuh"),
+    "rope": ("rope.cu", "tc_ptx.cuh", "common.cuh"),
+    "rotation_qk": ("rope.cu", "tc_ptx.cuh", "common.cuh"),
     "decode_fp8": ("decode.cu", "tc_ptx.cuh", "common.cuh"),
     "bwd_kv": ("backward_tc.cu", "tc_ptx.cuh", "common.cuh"),
     "bwd_q": ("backward_tc.cu", "tc_ptx.cuh", "common.cuh"),
 }
 TRAFFIC = {
     # kernel: (source hash, bytes per launch, what was captured)
-    "prefill_tc": ("ef5cbaad609205d0", 510.16e6 + 118.21e6,
+    "prefill_tc": ("b9f24d6a960fc613", 515.92e6 + 120.03e6,
                    "bench.py --part prefill: Llama-2-7B shape S=16384, one launch"),
-    "decode": ("6ccc745edbe73e16", 4.30e9 + 3.63e6,
+    "rotation_qk": ("f702d243b8631d22", 268.62e6 + 216.82e6,
+                    "bench.py --part prefill: the step's rotation pass over Q and K, one launch"),
+    "decode": ("28d4a32106eabc66", 4295.77e6 + 3.58e6,
                "bench.py --part decode: 64 sequences x 32 heads x 4096 slots, one launch"),
-    "decode_fp8": ("6ccc745edbe73e16", 2.15e9 + 3.55e6,
+    "decode_fp8": ("28d4a32106eabc66", 2148.42e6 + 3.65e6,
                    "bench.py --part decode_fp8: the same cache shape in FP8 E4M3, one launch"),
-    "rope": ("b80e2ddfaa08bdd0", 134.24e6 + 89.69e6,
+    "rope": ("f702d243b8631d22", 134.40e6 + 79.47e6,
              "bench.py --part rope: Q [1, 32, 16384, 128] bf16, one launch"),
-    "bwd_kv": ("ecd0a5c84e4bee9c", 550.20e6 + 240.68e6,
+    "bwd_kv": ("66006ddcc17da4c5", 550.66e6 + 240.62e6,
                "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
-    "bwd_q": ("ecd0a5c84e4bee9c", 557.30e6 + 116.45e6,
+    "bwd_q": ("66006ddcc17da4c5", 556.69e6 + 116.47e6,
               "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
 }
 
@@ -592,6 +595,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "pct_bf16_peak": {"burst": value / world / tf_burst, "sustained": value / world / tf_sust,
                           "peaks": peak_src},
+        "rotation_pass_traffic": traffic("rotation_qk"),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_burst, "unit": "TFLOP/s",
                      "frac": attn_tflops / tf_burst, "traffic": traffic("prefill_tc"),
                      "kernel": "prefill_tc_kernel alone on pre-rotated Q/K (the launch the step makes)",
