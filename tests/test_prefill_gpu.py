@@ -166,3 +166,23 @@ def test_perdim_scale_vector_prefill_all_rows():
         got.append(f64(o[0, h])); want.append(oo); gl.append(f64(lse[0, h])); wl.append(ll)
     assert_attn_close(np.concatenate(got), np.concatenate(want), "perdim")
     assert_lse_close(np.concatenate(gl), np.concatenate(wl), "perdim")
+
+
+def test_strided_inputs_all_rows():
+    """Q, K, V given as [B, S, H, d] tensors viewed as [B, H, S, d] (row
+    stride H * d): the rotation pass copies them row by row, V is read in place
+    through its strides; every row against the oracle, and the same result as
+    contiguous copies."""
+    need_cuda()
+    w = W.Prefill("strided", 63, 2, 4, 2, 300, 128, torch.bfloat16, W.RopeSpec("yarn", 1e4, 128, 0, 4.0), "causal")
+    q, k, v = W.prefill_inputs(w, "cuda")
+    qs, ks, vs = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (q, k, v))
+    assert qs.stride(2) == w.Hq * w.d and ks.stride(2) == w.Hkv * w.d
+    o, lse = api.attn_fwd_prefill(cfg_of(w), qs, ks, vs, return_lse=True)
+    o_c = api.attn_fwd_prefill(cfg_of(w), q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_c)
+    ref = oracle_prefill(w, q, k, v, 0)
+    got_o = np.concatenate([f64(o[b, h]) for (b, h) in ref])
+    want_o = np.concatenate([oo for (_, oo, _) in ref.values()])
+    assert_attn_close(got_o, want_o, "strided")
