@@ -57,6 +57,14 @@ struct DecodeShape {
   static constexpr int SMEM = 2 * NSTG * STAGE;
 };
 
+// 2^x (hardware approximation; relative error about 2^-22, results below
+// 2^-126 flushed to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float exp2_diff(float a, float b) {
   // 2^(a - b) with a = -inf giving 0.
   return a == -INFINITY ? 0.f : exp2f(a - b);
@@ -309,15 +317,20 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
 #pragma unroll
         for (int o = 1; o < TPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
         dot *= k_scale;
-        if (valid) {
-          if (dot > mrun[0] + kRescaleThreshold) {  // lazy: the reference moves rarely
-            const float corr = exp2_diff(mrun[0], dot);
-            lrun[0] *= corr;
+        // The rare move of the lazy reference is one warp-uniform branch
+        // instead of a divergent one per key.  Keys past the end (only in a
+        // slice's last chunk) are skipped: their stage bytes were not loaded.
+        const bool grow = valid && dot > mrun[0] + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float mnew = grow ? dot : mrun[0];
+          const float corr = exp2_diff(mrun[0], mnew);
+          lrun[0] *= corr;
 #pragma unroll
-            for (int k = 0; k < PPT; ++k) { acc1[0][k] *= corr; acc2[0][k] *= corr; }
-            mrun[0] = dot;
-          }
-          const float pr = exp2f(dot - mrun[0]);
+          for (int k = 0; k < PPT; ++k) { acc1[0][k] *= corr; acc2[0][k] *= corr; }
+          mrun[0] = mnew;
+        }
+        if (valid) {
+          const float pr = ex2(dot - mrun[0]);
           lrun[0] += pr;
 #pragma unroll
           for (int k = 0; k < PPT; k += 2) {

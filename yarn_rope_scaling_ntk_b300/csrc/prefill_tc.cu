@@ -424,17 +424,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
       if (needs_mask(p, my_r0, my_r1, n0)) {
+        // Visible columns of row m, as bounds on the column e (key position
+        // kp0 + n0 + e, query position qp0 + m): e <= hi (inside the chunk,
+        // inside the keys, not after the query) and, under the sink-window
+        // mask, a sink (e < s_end) or inside the window (e > w_lo).
+        const int ng0 = p.kp0 + n0, mg = p.qp0 + m;
+        int hi = min(p.cs, p.Skv - n0) - 1;
+        if (p.mask != YR_MASK_NONE) hi = min(hi, mg - ng0);
+        const bool sw = p.mask == YR_MASK_SINK_WINDOW;
+        const int s_end = sw ? p.sink - ng0 : BN;
+        const int w_lo = sw ? mg - p.window - ng0 : -1;
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          const int n = n0 + e;                           // local key index
-          bool vis = e < p.cs && n < p.Skv;
-          if (p.mask != YR_MASK_NONE) {
-            const int ng = p.kp0 + n, mg = p.qp0 + m;    // positions
-            vis = vis && ng <= mg;
-            if (p.mask == YR_MASK_SINK_WINDOW) vis = vis && (ng < p.sink || mg - ng < p.window);
-          }
-          if (!vis) x[e] = -INFINITY;
-        }
+        for (int e = 0; e < BN; ++e)
+          if (e > hi || (e >= s_end && e <= w_lo)) x[e] = -INFINITY;
       }
       // row max of the raw logits: eight independent 3-input chains
       float mx8[8];
