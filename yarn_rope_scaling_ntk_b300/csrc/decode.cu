@@ -40,6 +40,7 @@ constexpr int kWarps = 8;                    // compute warps
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int NSTG = 3;                      // shared-memory stages
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr int kReanchor = 16;                // chunks between exact rotation anchors (FP8 caches)
 
 // PPT rotation pairs per thread: 8 (two 16-byte vectors per key row) when
 // one query head shares the key, 4 when several do, so the per-thread query and
@@ -111,7 +112,8 @@ __device__ __forceinline__ void load_cache(const uint8_t* p, float (&x)[N]) {
 }
 
 template <int D, int G, int EB>
-__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(DecodeLaunch a, RopeFreqs f) {
+__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
+    decode_kernel(const __grid_constant__ DecodeLaunch a, const __grid_constant__ RopeFreqs f) {
   constexpr int PPT = G >= 2 ? 4 : 8;
   constexpr int QROW = D * 2;  // the query is bfloat16
   using Sh = DecodeShape<D, PPT, EB>;
@@ -265,26 +267,32 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1) decode_kernel(Decode
 
   bool ok = true;
   int c = 0;
+  float rc[PPT], rs_[PPT];   // cos / sin of (m - j) theta (kRotQ) or j theta
+  float qh1[PPT], qh2[PPT];  // kRotQ: the backward-rotated query
   for (int jc = j0; jc < j1; jc += CK, ++c) {
     const int s = c % NSTG;
     ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (c / NSTG) & 1, &abort_flag, status, 42, a.wait_limit));
     if (!ok) break;
     const uint8_t* stK = sK + s * Sh::STAGE;
     const uint8_t* stV = sV + s * Sh::STAGE;
-    // anchor of this chunk: the rotation for the thread's first key j_a
-    const int j_a = jc + warp * KPW + kg;
-    float rc[PPT], rs_[PPT];  // cos / sin of (m - j) theta (kRotQ) or j theta
+    // Anchor: the exact rotation for the thread's first key j_a of this
+    // chunk.  The recurrence steps by KPS positions per key, and the thread's
+    // first key of the next chunk is KPS after its last key of this one, so
+    // it carries over; it is re-anchored every kReanchor chunks, which keeps
+    // the drift of the rounded step rotation below about 10^-5.
+    if (!kRecur || c % kReanchor == 0) {
+      const int j_a = jc + warp * KPW + kg;
 #pragma unroll
-    for (int k = 0; k < PPT; ++k) {
-      if (identity || !kRecur) { rc[k] = 1.f; rs_[k] = 0.f; }
-      else turn_cos_sin<false>((float)(kRotQ ? mq - j_a : j_a), fr[k], rc[k], rs_[k]);
-    }
-    // kRotQ: the backward-rotated query itself is the recurrence state
-    float qh1[PPT], qh2[PPT];
+      for (int k = 0; k < PPT; ++k) {
+        if (identity || !kRecur) { rc[k] = 1.f; rs_[k] = 0.f; }
+        else turn_cos_sin<false>((float)(kRotQ ? mq - j_a : j_a), f.f[c8 * PPT + k], rc[k], rs_[k]);
+      }
+      // kRotQ: the backward-rotated query itself is the recurrence state
 #pragma unroll
-    for (int k = 0; k < PPT; ++k) {
-      qh1[k] = q1[0][k] * rc[k] - q2[0][k] * rs_[k];
-      qh2[k] = q1[0][k] * rs_[k] + q2[0][k] * rc[k];
+      for (int k = 0; k < PPT; ++k) {
+        qh1[k] = q1[0][k] * rc[k] - q2[0][k] * rs_[k];
+        qh2[k] = q1[0][k] * rs_[k] + q2[0][k] * rc[k];
+      }
     }
 #pragma unroll
     for (int u = 0; u < CK / KPS; ++u) {
