@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
 #pragma unroll
   for (int k = 0; k < PPT; ++k) {
     if (identity) { stc[k] = 1.f; sts[k] = 0.f; }
-    else turn_cos_sin<false>((float)KPS, fr[k], stc[k], sts[k]);
+    else turn_cos_sin<true>((float)KPS, fr[k], stc[k], sts[k]);  // precise: the step repeats
   }
   float nsts[PPT];
 #pragma unroll
