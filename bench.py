@@ -64,7 +64,7 @@ TRAFFIC = {
                "bench.py --part decode: 64 sequences x 32 heads x 4096 slots, one launch"),
     "decode_fp8": ("3f0f6b32031b2712", 2148.34e6 + 16.40e6,
                    "bench.py --part decode_fp8: the same cache shape in FP8 E4M3, one launch"),
-    "rope": ("recapture", 0.0,
+    "rope": ("f702d243b8631d22", 268.63e6 + 214.95e6,
              "bench.py --part rope: Q and K stacked, [1, 64, 16384, 128] bf16, one launch"),
     "bwd_kv": ("66006ddcc17da4c5", 550.66e6 + 240.62e6,
                "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
