@@ -59,7 +59,7 @@ struct BwdParams {
   int mask, sink, window;
   float scale_log2;  // scale * log2(e)
   float scale;       // softmax scale (applied to dQ and dK)
-  const float* lse2; // [B, Hq, S], LSE * log2(e)
+  const float* lse2; // [B, Hq, S], -LSE * log2(e)
   const float* dsum; // [B, Hq, S], rowsum(dO * O)
   void* out_a;       // dK (kv kernel) or dQ (q kernel)
   int64_t oas[3];
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < iters; ++i) {
       const int s = i % NS;
       const int m0 = (qlo + i % per_head) * BT;
-      const uint32_t vec = smem_u32(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);  // LSE*log2e | D
+      const uint32_t vec = smem_u32(smem + C::kvStage0 + s * C::kvStage + 2 * C::kTile);  // -LSE*log2e | D
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], i & 1, &abort_flag, p.status, 71));
       // the LSE / D vectors of this stage landed with full[s] (already
       // complete: the MMA waited for it before the products of s_full); the
@@ -421,17 +421,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q4 = 0; q4 < 16; ++q4) {  // 4 query columns per step
           const float4 l4 = lds_f4(vec + (col0 + 4 * q4) * 4);
           const float4 d4 = lds_f4(vec + 1024 + (col0 + 4 * q4) * 4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const float nl[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
           float pp[4], dd[4];
+          // two columns per packed op: P = 2^(S scale log2e - LSE log2e),
+          // dS = P (dP - D)
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
+          for (int t = 0; t < 4; t += 2) {
             const int e = 4 * q4 + t;  // column within the group's 64
-            const float sv = __uint_as_float(sr[e >> 5][e & 31]);
-            const float dv = __uint_as_float(dr[e >> 5][e & 31]);
-            float pr = ex2(fmaf(sv, sl2, -lv[t]));
-            if (decltype(masked)::value && (e < e_lo || e >= e_hi)) pr = 0.f;
-            pp[t] = pr;
-            dd[t] = pr * (dv - dvv[t]);
+            const float sv0 = __uint_as_float(sr[e >> 5][e & 31]), sv1 = __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]);
+            const float dv0 = __uint_as_float(dr[e >> 5][e & 31]), dv1 = __uint_as_float(dr[(e + 1) >> 5][(e + 1) & 31]);
+            float a0, a1, g0, g1;
+            fma2(a0, a1, sv0, sv1, sl2, sl2, nl[t], nl[t + 1]);
+            float p0 = ex2(a0), p1 = ex2(a1);
+            if (decltype(masked)::value) {
+              if (e < e_lo || e >= e_hi) p0 = 0.f;
+              if (e + 1 < e_lo || e + 1 >= e_hi) p1 = 0.f;
+            }
+            fma2(g0, g1, dvv[t], dvv[t + 1], -1.f, -1.f, dv0, dv1);
+            mul2(dd[t], dd[t + 1], p0, p1, g0, g1);
+            pp[t] = p0;
+            pp[t + 1] = p1;
           }
           pk[2 * q4] = pack_bf16(pp[0], pp[1]);
           pk[2 * q4 + 1] = pack_bf16(pp[2], pp[3]);
@@ -650,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int col0 = wg * 64;
     const int64_t row = ((int64_t)b * p.Hq + hq) * p.S + m;
-    const float lse_l2 = p.lse2[row];
+    const float nlse_l2 = p.lse2[row];  // -LSE * log2(e)
     const float dsum = p.dsum[row];
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -684,17 +693,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto softmax = [&](auto masked) {
 #pragma unroll
         for (int e2 = 0; e2 < 32; ++e2) {
-          float dd[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int e = 2 * e2 + t;
-            const float sv = __uint_as_float(sr[e >> 5][e & 31]);
-            const float dv = __uint_as_float(dr[e >> 5][e & 31]);
-            float pr = ex2(fmaf(sv, sl2, -lse_l2));
-            if (decltype(masked)::value && (e > e_max || (e >= e_sink && e <= e_win))) pr = 0.f;
-            dd[t] = pr * (dv - dsum);
+          // two columns per packed op: P = 2^(S scale log2e - LSE log2e),
+          // dS = P (dP - D)
+          const int e = 2 * e2;
+          const float sv0 = __uint_as_float(sr[e >> 5][e & 31]), sv1 = __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]);
+          const float dv0 = __uint_as_float(dr[e >> 5][e & 31]), dv1 = __uint_as_float(dr[(e + 1) >> 5][(e + 1) & 31]);
+          float a0, a1, g0, g1, d0, d1;
+          fma2(a0, a1, sv0, sv1, sl2, sl2, nlse_l2, nlse_l2);
+          float p0 = ex2(a0), p1 = ex2(a1);
+          if (decltype(masked)::value) {
+            if (e > e_max || (e >= e_sink && e <= e_win)) p0 = 0.f;
+            if (e + 1 > e_max || (e + 1 >= e_sink && e + 1 <= e_win)) p1 = 0.f;
           }
-          dk[e2] = pack_bf16(dd[0], dd[1]);
+          fma2(g0, g1, dsum, dsum, -1.f, -1.f, dv0, dv1);
+          mul2(d0, d1, p0, p1, g0, g1);
+          dk[e2] = pack_bf16(d0, d1);
         }
       };
       if (need_mask) softmax(std::true_type{});
@@ -738,7 +751,7 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, fl
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
     dsum[row] = acc;
-    lse2[row] = lse[row] * kLog2e;
+    lse2[row] = -lse[row] * kLog2e;
   }
 }
 

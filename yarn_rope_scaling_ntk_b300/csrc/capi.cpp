@@ -389,7 +389,7 @@ size_t yr_bwd_workspace_bytes(const yr_rope_cfg* cfg, int32_t in_dtype, int32_t 
   const size_t q = (size_t)B * Hq * S * d * 2, kv = (size_t)B * Hkv * S * d * 2;
   size_t bytes = align16(q) + align16(kv);                   // rotated Q, K
   if (in_dtype == YR_F32) bytes += align16(kv) + align16(q);  // bf16 V, dO
-  bytes += 2 * align16((size_t)B * Hq * S * 4);              // D = rowsum(dO * O), LSE * log2(e)
+  bytes += 2 * align16((size_t)B * Hq * S * 4);              // D = rowsum(dO * O), -LSE * log2(e)
   return bytes;
 }
 

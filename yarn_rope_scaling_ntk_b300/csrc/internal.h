@@ -131,7 +131,7 @@ struct BwdLaunch {
   const void* k;
   const void* v;
   const void* dout;
-  const float* lse2;  // LSE * log2(e)
+  const float* lse2;  // -LSE * log2(e)
   const float* dsum;
   void* dq;
   void* dk;
@@ -145,7 +145,7 @@ struct BwdLaunch {
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 // D = rowsum(dO * O) of [B, H, S, d] tensors (bf16 when bf16 != 0, else f32),
-// and lse2 = lse * log2(e) for the same rows.
+// and lse2 = -lse * log2(e) for the same rows.
 cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, const float* lse, float* lse2, int B,
                         int H, int S, int d, const int64_t ds[3], const int64_t os[3], cudaStream_t st);
 
