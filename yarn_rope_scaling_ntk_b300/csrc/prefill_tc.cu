@@ -460,15 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float corr = rescale ? ex2(m_used - mx) : 1.0f;
       if (grow) m_used = mx;
       const float neg_ref = m_used == -INFINITY ? 0.f : -m_used;
+      // two columns per packed op: the exponent argument and the row sum
+      // (four partial sums, two packed chains)
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float a0 = ex2(fmaf(x[c * 64 + 2 * e], sc, neg_ref));
-          const float a1 = ex2(fmaf(x[c * 64 + 2 * e + 1], sc, neg_ref));
-          sum4[e & 3] += a0 + a1;
+          float t0, t1;
+          fma2(t0, t1, x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1], sc, sc, neg_ref, neg_ref);
+          const float a0 = ex2(t0), a1 = ex2(t1);
+          const int j = 2 * (e & 1);
+          fma2(sum4[j], sum4[j + 1], a0, a1, 1.f, 1.f, sum4[j], sum4[j + 1]);
           pk[e] = pack_bf16(a0, a1);
         }
         tmem_st32(s_addr + c * 32, pk);
