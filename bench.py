@@ -13,6 +13,8 @@ workload's Q and K, reported as sub-objects.
 
 ``--impl reference`` times the float64 CPU oracle on a bounded sample of the
 same workload (the oracle is the reference arm: the pages ship no code).
+``--ring`` times ring attention over the N ranks on the 131072-token
+workload instead (one KV block per rank, NCCL point-to-point exchange).
 """
 
 from __future__ import annotations
@@ -702,6 +704,132 @@ def run_part(args):
     print(json.dumps({"part": args.part, "small": args.small, "calls": n}))
 
 
+def _ring_check_ops(rank: int, world: int, seen: list):
+    """Ring operations that do no attention, for the CPU check of the ring
+    launch: every K block carries its block index as its value; ``block``
+    records the index it was given and returns an empty partial, and the
+    rotation and the merge leave their inputs as they are."""
+    from yarn_rope_scaling_ntk_b300 import ring
+
+    def rotate(cfg, x, pos0):
+        return x
+
+    def block(q, k, v, q_pos0, k_pos0, mask, sink, window, scale, out_dtype):
+        seen.append((int(k.flatten()[0].item()), k_pos0))
+        o = torch.zeros(q.shape, dtype=out_dtype)
+        return o, torch.full(q.shape[:3], -math.inf, dtype=torch.float32)
+
+    def merge(o_acc, lse_acc, o_part, lse_part, out):
+        pass
+
+    return ring.RingOps(rotate, block, merge)
+
+
+def run_ring(args):
+    """``--ring``: the long-sequence workload (B=1, H=32, S=131072, d=128,
+    YaRN s=32, causal) as ring attention over the job's N ranks.  Rank I
+    holds query and KV block I of S / N tokens; every step rotates its Q and
+    K, passes KV blocks around the ring with ``torch.distributed``
+    point-to-point transfers (NCCL) overlapped with the block attention, and
+    merges the partials.  The total work is fixed as N grows (strong
+    scaling); the value is the whole sequence's attention FLOPs over the
+    slowest rank's time.  With ``--launcher-check`` the ranks join a gloo
+    group on the CPU and run the exchange with operations that do no
+    attention, checking that each rank is handed the blocks of the ring
+    order (no GPU work)."""
+    from yarn_rope_scaling_ntk_b300 import ring
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.RING_128K
+    cfg = cfg_of(w)
+    if w.S % (world * 128):
+        raise SystemExit(f"--ring needs S = {w.S} to split into {world} blocks of a multiple of 128 tokens")
+    bs = w.S // world
+    import torch.distributed as dist
+    if args.launcher_check:
+        if world > 1:
+            dist.init_process_group("gloo", rank=rank, world_size=world)
+        kb = torch.full((1, 1, 128, 64), float(rank), dtype=torch.float64)
+        ok = True
+        for _ in range(max(1, args.steps)):
+            seen = []
+            ops = _ring_check_ops(rank, world, seen)
+            small = api.RopeConfig(kind="none", head_dim=64)
+            if world > 1:
+                ring.ring_attention(small, kb.clone(), kb.clone(), kb.clone(), mask="causal", ops=ops)
+            else:
+                ring.ring_attention_one_process(small, [kb], [kb], [kb], mask="causal", ops=ops)
+            want = [(j, j * 128) for j in (ring.held_block(rank, t, world) for t in range(world)) if j <= rank]
+            ok = ok and seen == want
+        flag = torch.tensor([1.0 if ok else 0.0], dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(flag, op=dist.ReduceOp.MIN)
+        if rank == 0:
+            print(json.dumps({"launcher_check": True, "mode": "ring", "n_gpus": world,
+                              "ring_order_ok": bool(flag.item() == 1.0), "steps": args.steps}))
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    q, k, v = W.prefill_inputs(w, dev)
+    sl = slice(rank * bs, (rank + 1) * bs)
+    qb, kb, vb = (t[:, :, sl].contiguous() for t in (q, k, v))
+    del q, k, v
+    torch.cuda.empty_cache()
+
+    def step():
+        if world > 1:
+            return ring.ring_attention(cfg, qb, kb, vb, mask=w.mask)
+        return ring.ring_attention_one_process(cfg, [qb], [kb], [vb], mask=w.mask)[0]
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    api.sync_status()
+
+    def fence():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    fence()
+    n0 = api.kernel_launch_count()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        fence()
+    launches = api.kernel_launch_count() - n0
+    api.sync_status()
+    ms = a.elapsed_time(b)
+    mx = reduce_max(ms, dist if world > 1 else None, dev)
+    mn = -reduce_max(-ms, dist if world > 1 else None, dev)
+    flops = prefill_flops(w)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "ring attention TFLOP/s (causal, whole sequence over all ranks)", "mode": "ring",
+            "value": flops * args.steps / (mx * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": mx / args.steps,
+            "ms_per_step_fastest_rank": mn / args.steps, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.Hq, "S": w.S, "d": w.d, "mask": w.mask,
+                       "block_tokens": bs, "parallelism": f"ring{world}",
+                       "exchange": "torch.distributed batch_isend_irecv (NCCL)" if world > 1 else "none (one rank)",
+                       "l2": "inputs larger than L2"},
+            "clocks": clk.summary(), "gpu_launches": launches,
+        }))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def _free_port() -> int:
     import socket
     with socket.socket() as sk:
@@ -768,11 +896,15 @@ def _parse(argv):
     ap.add_argument("--small", action="store_true", help="with --part: smaller workload")
     ap.add_argument("--launcher-check", action="store_true",
                     help="start the ranks on CPU (gloo) and print one line per job, no GPU work")
+    ap.add_argument("--ring", action="store_true",
+                    help="ring attention over the N ranks on the 131072-token workload (strong scaling)")
     return ap.parse_args(argv)
 
 
 def _dispatch(args):
-    if args.launcher_check:
+    if args.ring and args.impl == "ours" and not args.part:
+        run_ring(args)
+    elif args.launcher_check:
         run_launcher_check(args)
     elif args.part:
         run_part(args)

@@ -80,3 +80,14 @@ def test_bench_under_a_launcher_does_not_start_ranks_again():
     env = dict(os.environ, RANK="0", LOCAL_RANK="0", WORLD_SIZE="1")
     lines = _bench_lines("--gpus", "2", "--steps", "2", "--launcher-check", env=env)
     assert len(lines) == 1 and lines[0]["n_gpus"] == 1
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_bench_ring_mode_starts_n_ranks_and_hands_each_the_ring_order(n):
+    """``bench.py --ring --gpus N``: N ranks pass their KV blocks around the
+    ring (gloo point-to-point on the CPU here) and each rank is handed, at
+    step t, block (rank - t) mod N, skipping future blocks."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    lines = _bench_lines("--ring", "--gpus", str(n), "--steps", "2", "--launcher-check", env=env)
+    assert len(lines) == 1
+    assert lines[0]["mode"] == "ring" and lines[0]["n_gpus"] == n and lines[0]["ring_order_ok"] is True
