@@ -62,25 +62,31 @@ def test_kv_block_against_oracle(mask, sink, window, q_pos0, k_pos0, Sq, Skv):
     assert_lse_close(f64(lse), want_l, f"kv block {mask}")
 
 
-def test_merge_kernel_against_oracle():
+@pytest.mark.parametrize("B,H,S,d,final_dtype", [(2, 3, 70, 128, torch.bfloat16),
+                                                  (1, 5, 1001, 64, torch.float32),    # ragged row groups
+                                                  (1, 2, 9, 256, torch.bfloat16)])    # two chunks per row
+def test_merge_kernel_against_oracle(B, H, S, d, final_dtype):
+    """Merge of two partials against the oracle's combination, with empty
+    accumulator rows (NaN contents never read), empty partials and rows
+    empty on both sides; rows taken several per warp in a grid-stride loop."""
     need_cuda()
-    B, H, S, d = 2, 3, 70, 128
-    g = torch.Generator(device="cuda").manual_seed(5)
+    g = torch.Generator(device="cuda").manual_seed(5 + d)
     oa = torch.randn(B, H, S, d, generator=g, device="cuda")
     ob = torch.randn(B, H, S, d, generator=g, device="cuda")
     la = torch.randn(B, H, S, generator=g, device="cuda") * 3
     lb = torch.randn(B, H, S, generator=g, device="cuda") * 3
-    la[0, 0, :5] = -math.inf       # accumulator empty: its O is never read
-    oa[0, 0, :5] = float("nan")
-    lb[1, 2, 10:20] = -math.inf    # partial empty
-    la[1, 1, 30] = lb[1, 1, 30] = -math.inf   # both empty
+    n = B * H * S
+    la.view(-1)[:5] = -math.inf               # accumulator empty: its O is never read
+    oa.view(n, d)[:5] = float("nan")
+    lb.view(-1)[n // 2:n // 2 + 4] = -math.inf  # partial empty
+    la.view(-1)[n - 1] = lb.view(-1)[n - 1] = -math.inf   # both empty
     want_o, want_l = [], []
     for b in range(B):
         for h in range(H):
             o, l = A.merge_partials([(f64(oa[b, h]), f64(la[b, h])), (f64(ob[b, h]), f64(lb[b, h]))])
             want_o.append(o)
             want_l.append(l)
-    final = torch.empty(B, H, S, d, dtype=torch.bfloat16, device="cuda")
+    final = torch.empty(B, H, S, d, dtype=final_dtype, device="cuda")
     api.attn_merge_partial(oa, la, ob, lb, out=final)
     torch.cuda.synchronize()
     got_o = f64(oa).reshape(-1, S, d)
@@ -89,7 +95,7 @@ def test_merge_kernel_against_oracle():
     gl, wl = f64(la).reshape(-1, S), np.stack(want_l)
     assert np.array_equal(np.isneginf(gl), np.isneginf(wl))
     np.testing.assert_allclose(np.where(np.isneginf(gl), 0, gl), np.where(np.isneginf(wl), 0, wl), atol=1e-5)
-    assert torch.equal(final, oa.to(torch.bfloat16))
+    assert torch.equal(final, oa.to(final_dtype))
 
 
 @pytest.mark.parametrize("mask,sink,window", [("causal", 0, 0), ("sink_window", 4, 300)])
