@@ -731,25 +731,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// D = rowsum(dO * O): one warp per row of [B, H, S, d].
+// D = rowsum(dO * O) of [B, H, S, d] and lse2 = -LSE * log2(e) per row.  Each
+// lane takes 16 contiguous bytes of a row of both tensors (8 bf16 or 4
+// float32 elements), d / that many lanes share a row, so one warp covers
+// 32 / (lanes per row) rows with one 16-byte load of each tensor per lane.
 template <typename T>
 __global__ void __launch_bounds__(256) dsum_kernel(const T* dout, const T* o, float* dsum, const float* lse,
                                                    float* lse2, int B, int H, int S, int d, int64_t ds0, int64_t ds1,
                                                    int64_t ds2, int64_t os0, int64_t os1, int64_t os2) {
+  constexpr int EPL = 16 / (int)sizeof(T);  // elements per lane
   const int64_t rows = (int64_t)B * H * S;
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const int s = (int)(row % S);
-  const int64_t bh = row / S;
-  const int h = (int)(bh % H), b = (int)(bh / H);
-  const T* dr = dout + b * ds0 + h * ds1 + (int64_t)s * ds2;
-  const T* orow = o + b * os0 + h * os1 + (int64_t)s * os2;
+  const int lpr = d / EPL;  // lanes per row: 8, 16 or 32 (d = 64 or 128)
+  const int64_t row = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * (32 / lpr) + lane / lpr;
+  const int sub = lane % lpr;
   float acc = 0.f;
-  for (int c = lane; c < d; c += 32) acc = fmaf(static_cast<float>(dr[c]), static_cast<float>(orow[c]), acc);
+  if (row < rows) {
+    const int s = (int)(row % S);
+    const int64_t bh = row / S;
+    const int h = (int)(bh % H), b = (int)(bh / H);
+    const uint4 x = *reinterpret_cast<const uint4*>(dout + b * ds0 + h * ds1 + (int64_t)s * ds2 + sub * EPL);
+    const uint4 y = *reinterpret_cast<const uint4*>(o + b * os0 + h * os1 + (int64_t)s * os2 + sub * EPL);
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+    for (int j = 0; j < 4; ++j) {
+      if constexpr (sizeof(T) == 2) {  // bf16 pairs: the low half is the even element
+        acc = fmaf(__uint_as_float(xw[j] << 16), __uint_as_float(yw[j] << 16), acc);
+        acc = fmaf(__uint_as_float(xw[j] & 0xffff0000u), __uint_as_float(yw[j] & 0xffff0000u), acc);
+      } else {
+        acc = fmaf(__uint_as_float(xw[j]), __uint_as_float(yw[j]), acc);
+      }
+    }
+  }
+  for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
     dsum[row] = acc;
     lse2[row] = -lse[row] * kLog2e;
   }
@@ -800,7 +815,10 @@ cudaError_t launch_dsum(const void* dout, const void* o, int bf16, float* dsum, 
                         int H, int S, int d, const int64_t ds[3], const int64_t os[3], cudaStream_t st) {
   const int64_t rows = (int64_t)B * H * S;
   if (rows == 0) return cudaSuccess;
-  const int64_t blocks = (rows + 7) / 8;
+  if (d != 64 && d != 128) return cudaErrorInvalidValue;
+  const int lpr = d / (bf16 ? 8 : 4);
+  const int64_t warps = (rows + 32 / lpr - 1) / (32 / lpr);
+  const int64_t blocks = (warps + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (bf16)
     dsum_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
