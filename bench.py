@@ -68,9 +68,9 @@ TRAFFIC = {
                    "bench.py --part decode_fp8: the same cache shape in FP8 E4M3, one launch"),
     "rope": ("f702d243b8631d22", 268.63e6 + 214.95e6,
              "bench.py --part rope: Q and K stacked, [1, 64, 16384, 128] bf16, one launch"),
-    "bwd_kv": ("11e31f293ef4db0d", 550.37e6 + 241.05e6,
+    "bwd_kv": ("9631e3af16d2f5fe", 550.11e6 + 237.83e6,
                "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
-    "bwd_q": ("11e31f293ef4db0d", 556.71e6 + 116.43e6,
+    "bwd_q": ("9631e3af16d2f5fe", 557.85e6 + 116.88e6,
               "bench.py --part backward: Llama-2-7B shape S=16384, one launch"),
 }
 
