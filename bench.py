@@ -704,7 +704,7 @@ def run_part(args):
     print(json.dumps({"part": args.part, "small": args.small, "calls": n}))
 
 
-def _ring_check_ops(rank: int, world: int, seen: list):
+def _ring_check_ops(seen: list):
     """Ring operations that do no attention, for the CPU check of the ring
     launch: every K block carries its block index as its value; ``block``
     records the index it was given and returns an empty partial, and the
@@ -754,7 +754,7 @@ def run_ring(args):
         ok = True
         for _ in range(max(1, args.steps)):
             seen = []
-            ops = _ring_check_ops(rank, world, seen)
+            ops = _ring_check_ops(seen)
             small = api.RopeConfig(kind="none", head_dim=64)
             if world > 1:
                 ring.ring_attention(small, kb.clone(), kb.clone(), kb.clone(), mask="causal", ops=ops)
