@@ -128,6 +128,35 @@ def test_empty_inputs_return_ok_without_launch(lib):
     assert st == 0
 
 
+def test_every_entry_point_accepts_empty_inputs(lib):
+    """A zero batch or a zero length is a valid call with nothing to do: each
+    entry point returns YR_OK before it touches a pointer or launches."""
+    cfg = api.RopeConfig(kind="yarn", head_dim=128, L_train=4096, s=4.0).c()
+    z = lambda: _i64(0, 0, 0)
+    n0 = lib.yr_kernel_launch_count()
+    # prefill: B = 0
+    assert lib.attn_fwd_prefill(ctypes.byref(cfg), None, None, None, None, None, 1, 0, 4, 4, 256, 128,
+                                z(), z(), z(), z(), 0, 0, 0, 1, 0.0, None, 0, None) == 0
+    # one KV block with no queries (a block with queries but no keys is not
+    # empty: it writes o = 0 and lse = -inf, and needs its pointers)
+    none = api.RopeConfig(kind="none", head_dim=128).c()
+    assert lib.attn_fwd_prefill_kv_block(ctypes.byref(none), None, None, None, None, None, 1, 0, 1, 4, 4, 0, 128,
+                                         128, 0, 0, z(), z(), z(), z(), 0, 0, 0, 0.0, None, 0, None) == 0
+    assert lib.attn_fwd_prefill_kv_block(ctypes.byref(none), None, None, None, None, None, 1, 0, 1, 4, 4, 128, 0,
+                                         128, 0, 0, z(), z(), z(), z(), 0, 0, 0, 0.0, None, 0, None) == 1
+    # decode, bf16 and FP8 caches: B = 0
+    assert lib.attn_fwd_decode_sinkwindow(ctypes.byref(cfg), None, None, None, None, None, 0, 32, 8, 128, 4,
+                                          4092, None, None, 0, None, 0, None) == 0
+    assert lib.attn_fwd_decode_sinkwindow_fp8(ctypes.byref(cfg), None, None, None, None, None, None, None, 0, 32,
+                                              8, 128, 4, 4092, None, None, 0, None, 0, None) == 0
+    # merge: S = 0
+    assert lib.attn_merge_partial(None, None, None, None, None, 0, 1, 4, 0, 128, z(), z(), z(), None) == 0
+    # backward: S = 0
+    assert lib.attn_bwd(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, 1, 1, 1, 4, 4, 0,
+                        128, z(), z(), z(), z(), z(), z(), z(), z(), 0, 0, 0, 0.0, None, 0, None) == 0
+    assert lib.yr_kernel_launch_count() == n0
+
+
 def test_workspace_sizes(lib):
     cfg = api.RopeConfig(kind="yarn", head_dim=128, L_train=4096, s=4.0)
     assert api.prefill_workspace_bytes(cfg, torch.bfloat16, 1, 32, 8, 1024, 128) >= 8 * 1024 * 128 * 2
