@@ -47,3 +47,16 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     """Spacing of bfloat16 numbers at |x| (8 significant bits)."""
     ax = np.maximum(np.abs(x), 2.0 ** -126)
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def rope_bf16_bound(want: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """Bar for a bfloat16 rotation output: one bf16 ulp of the float64 value,
+    plus the float32 error of the rotation itself.  Each output is a two-term
+    sum x_i cos - x_(i+d/2) sin (or x_i sin + x_(i+d/2) cos) formed in float32
+    from an angle carried to a few float32 ulps, so its absolute error scales
+    with |x_i| + |x_(i+d/2)|, not with the output: 2^-20 of that sum (16
+    float32 ulps) covers it.  Where the two terms nearly cancel, the output's
+    own ulp is far smaller than that error; elsewhere the ulp dominates."""
+    h = x.shape[-1] // 2
+    pair = np.abs(x[..., :h]) + np.abs(x[..., h:])
+    return bf16_ulp(want) + 2.0 ** -20 * np.concatenate([pair, pair], axis=-1)

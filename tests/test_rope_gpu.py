@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle.rope as R
-from tests.helpers import ROPE_F32_ATOL, bf16_ulp, f64, gpu, need_cuda
+from tests.helpers import ROPE_F32_ATOL, f64, gpu, need_cuda, rope_bf16_bound
 from yarn_rope_scaling_ntk_b300 import api, workloads as W
 
 pytestmark = gpu
@@ -58,7 +58,25 @@ def test_rope_bf16_within_one_ulp(wl):
     th, _, _ = R.inv_freq(wl.rope.kind, wl.d, wl.rope.theta_base, wl.rope.L_train, wl.rope.L_target)
     want = R.rotate(f64(x[:, :, rows]), rows.numpy(), th)
     got = f64(y[:, :, rows])
-    assert np.all(np.abs(got - want) <= bf16_ulp(want) + 1e-6)
+    assert np.all(np.abs(got - want) <= rope_bf16_bound(want, f64(x[:, :, rows])))
+
+
+def test_rope_bench_launch_q_and_k_stacked():
+    """The launch the bench times: Q and K of the Llama-2-7B-shaped workload
+    stacked along the heads, [1, 64, 16384, 128] bf16, in one call; sampled
+    rows of every head within the bf16 rotation bar of the oracle."""
+    need_cuda()
+    wl = W.LLAMA2_7B
+    q, k, _ = W.prefill_inputs(wl, "cuda")
+    qk = torch.cat([q, k], dim=1)
+    cfg = _cfg(wl.rope.kind, wl.d, wl.rope.theta_base, wl.rope.L_train, wl.rope.L_target)
+    y = api.rope_apply(cfg, qk)
+    rows = W.sample_rows(wl.S, 512, wl.index + 7, extra=(wl.S // 2,))
+    th, _, _ = R.inv_freq(wl.rope.kind, wl.d, wl.rope.theta_base, wl.rope.L_train, wl.rope.L_target)
+    want = R.rotate(f64(qk[:, :, rows]), rows.numpy(), th)
+    got = f64(y[:, :, rows])
+    assert got.shape == (1, 2 * wl.Hq, len(rows), wl.d)
+    assert np.all(np.abs(got - want) <= rope_bf16_bound(want, f64(qk[:, :, rows])))
 
 
 def test_rope_positions_pos0_inplace_and_strides():
