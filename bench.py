@@ -132,6 +132,13 @@ def whole_job_rate(work_per_step: float, steps: int, world: int, max_total_ms: f
     return work_per_step * steps * world / (max_total_ms * 1e-3)
 
 
+def step_config(w, n: int) -> dict:
+    """The `config` object of the step's line, the same for both arms."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+            "mask": w.mask, "rope": "yarn s=4 L_train=4096 theta_base=1e4",
+            "l2": "inputs larger than L2 (537 MB Q/K/V/O vs 126 MB)", "parallelism": f"replicas x{n}"}
+
+
 def cfg_of(w):
     r = w.rope
     return api.RopeConfig(kind=r.kind, head_dim=w.d, theta_base=r.theta_base, L_train=r.L_train,
@@ -395,8 +402,7 @@ def run_reference(args):
             "full_workload_ms_extrapolated": full_ms,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
-                       "mask": w.mask, "rope": "yarn s=4 L_train=4096 theta_base=1e4"},
+            "config": step_config(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -603,10 +609,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
-                   "mask": w.mask, "rope": "yarn s=4 L_train=4096 theta_base=1e4",
-                   "l2": "inputs larger than L2 (537 MB Q/K/V/O vs 126 MB)",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(w, world),
         "pct_bf16_peak": {"burst": value / world / tf_burst, "sustained": value / world / tf_sust,
                           "peaks": peak_src},
         "rotation_pass_traffic": traffic("rotation_qk"),

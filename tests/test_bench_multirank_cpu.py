@@ -91,3 +91,17 @@ def test_bench_ring_mode_starts_n_ranks_and_hands_each_the_ring_order(n):
     lines = _bench_lines("--ring", "--gpus", str(n), "--steps", "2", "--launcher-check", env=env)
     assert len(lines) == 1
     assert lines[0]["mode"] == "ring" and lines[0]["n_gpus"] == n and lines[0]["ring_order_ok"] is True
+
+
+def test_reference_arm_line_matches_the_step_config():
+    """``bench.py --impl reference`` (the float64 oracle on the host cores)
+    prints one line with the same metric, unit and config as the GPU arm."""
+    import bench
+    from yarn_rope_scaling_ntk_b300 import workloads as W
+    lines = _bench_lines("--impl", "reference", "--steps", "1", "--warmup", "0")
+    assert len(lines) == 1
+    ln = lines[0]
+    assert ln["impl"] == "reference" and ln["metric"] == bench.METRIC and ln["unit"] == "TFLOP/s"
+    assert ln["config"] == bench.step_config(W.LLAMA2_7B, 1)
+    assert ln["value"] > 0 and ln["ms_per_step"] > 0 and ln["cpu_baseline"]["kind"] == "oracle"
+    assert ln["e2e"]["h2d_bytes_per_step"] == 0 and ln["e2e"]["d2h_bytes_per_step"] == 0
